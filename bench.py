@@ -1,0 +1,440 @@
+#!/usr/bin/env python3
+"""Benchmark: MoE route top-k -> dispatch count -> dispatch pack -> combine.
+
+One step is one pass of the whole routing path over one batch of the
+DeepSeek-V3-shaped decode workload (N=32 ranks x T=128 tokens, E=256, R=8,
+H=7168 bf16), with the inputs already in HBM.  The expert op between pack
+and combine stands in for the grouped expert GEMM and is not timed; in its
+place the L2 is flushed (a GPU-side write of 2x the L2 size), as it is
+before every step, so no kernel reads data a previous kernel left in L2.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on
+the host cores instead (bounded samples of the same workload).
+With N > 1 (torchrun) every rank runs an independent replica: the path has
+no exchange step across GPUs, so value = N * tokens / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (fraction of GB300 peak), 1 GPU"
+DEFAULT_WORKLOAD = "dsv3_decode"
+KERNELS = ("route", "count", "pack", "combine")
+KERNEL_SOURCES = {"route": "route_topk.cu", "count": "dispatch_count.cu",
+                  "pack": "dispatch_pack.cu", "combine": "combine.cu"}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--e2e-steps", type=int, default=100)
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="CPU work for the oracle baseline (0 disables it)")
+    p.add_argument("--no-clocks", action="store_true")
+    return p.parse_args()
+
+
+# --------------------------------------------------------------------------
+# helpers
+# --------------------------------------------------------------------------
+
+def dist_info():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def source_hash(name: str) -> str:
+    path = os.path.join(ROOT, "combine_moe_route_topk_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current source of that kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload, {}).get(kernel)
+    if not e or e.get("source_sha256_16") != source_hash(KERNEL_SOURCES[kernel]):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled in the background."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 20):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", f"-lms={period_ms}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def wait_first(self, timeout=10.0):
+        t0 = time.time()
+        while self.proc is not None and not self.samples and time.time() - t0 < timeout:
+            time.sleep(0.02)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [s for (t, s) in self.samples if t0 <= t <= t1 and len(s) >= 9]
+        if not rows:  # very short window: take the samples closest to it
+            rows = [s for (t, s) in self.samples if t0 - 0.5 <= t <= t1 + 0.5 and len(s) >= 9]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(rows[0][2]), "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timing (baseline / reference arm)
+# --------------------------------------------------------------------------
+
+def oracle_pass(w, inp, tokens=None):
+    """One oracle pass of route -> count -> pack -> combine (identity expert)
+    over the whole batch, or over the first `tokens` tokens treated as a
+    smaller batch of the same shape (T' = tokens / N per rank)."""
+    import numpy as np
+    import oracle
+    logits, bias = inp.logits.numpy(), None if inp.bias is None else inp.bias.numpy()
+    xb = oracle.x_as_bytes(inp.x)
+    T = w.T
+    if tokens is not None:
+        T = max(1, tokens // w.N)
+        logits, xb = logits[:w.N * T], xb[:w.N * T]
+    idx, tw, _ = oracle.route(logits, bias, w.R, w.score_fn, w.renormalize)
+    cap = w.N * T * max(w.R, w.E // w.N)
+    cnt, _ = oracle.count(w.N, T, w.E, cap, idx)
+    px, _, _ = oracle.pack(xb, None, cnt["pos"], cnt["rank_offsets"], cap)
+    y = px.view(np.uint16) if w.y_dtype == 0 else px.view(np.float32)
+    oracle.combine(y, w.y_dtype, cnt["pos"], cnt["rank_offsets"], tw, cap, w.H)
+    return w.N * T
+
+
+def cpu_baseline(w, inp, seconds):
+    n_tok, passes = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        n_tok += oracle_pass(w, inp)
+        passes += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": n_tok / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{passes} full pass(es) of the {w.name} batch ({w.NT} tokens): "
+                      f"route, count, pack, combine; single-threaded C, {dt:.1f} s"}
+
+
+def run_reference(args):
+    rank, _, world = dist_info()
+    if rank != 0:
+        return 0
+    import torch  # noqa: F401  (seeded generator)
+    from combine_moe_route_topk_gb300 import workloads as W
+    import oracle
+    oracle.build_lib()
+    w = W.WORKLOADS[args.workload]
+    inp = W.make_inputs(w)
+    # size the sample so the whole run stays within ~2 minutes
+    probe = 256
+    t0 = time.perf_counter()
+    oracle_pass(w, inp, probe)
+    per_tok = (time.perf_counter() - t0) / probe
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    sample = int(min(w.NT, max(w.N, (budget / per_tok) // w.N * w.N)))
+    for _ in range(args.warmup):
+        oracle_pass(w, inp, sample)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        n = oracle_pass(w, inp, sample)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.mean(times)
+    value = n / (ms / 1e3)
+    desc = (f"batches of {n} tokens ({n // w.N} per rank) of the {w.name} shape: route, count, "
+            f"pack, combine; single-threaded C oracle")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }))
+    return 0
+
+
+def workload_config(w):
+    from combine_moe_route_topk_gb300 import workloads as W
+    return {"workload": w.name, "N": w.N, "T": w.T, "tokens": w.NT, "E": w.E, "R": w.R,
+            "H": w.H, "x_dtype": {0: "bf16", 1: "f32", 2: "fp8e4m3+f32/128"}[w.x_dtype],
+            "scores": ("softmax" if w.score_fn == W.SOFTMAX else "sigmoid")
+                      + ("+renorm" if w.renormalize else ""),
+            "cap_rows_per_rank": W.default_cap(w),
+            "l2": "flushed before every step and between pack and combine (2x L2 write, untimed)",
+            "expert_op": "not timed (stands in for the grouped expert GEMM)",
+            "parallelism": "replicas"}
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import combine_moe_route_topk_gb300 as moe
+    from combine_moe_route_topk_gb300 import workloads as W
+
+    rank, local_rank, world = dist_info()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    moe.lib()  # fails loudly if the library was not built
+
+    w = W.WORKLOADS[args.workload]
+    dims = moe.dims_of(w)
+    inp_cpu = W.make_inputs(w)
+    inp = W.Inputs(*(t.to(dev) if t is not None else None
+                     for t in (inp_cpu.logits, inp_cpu.bias, inp_cpu.x, inp_cpu.x_scales)))
+    b = moe.Buffers(dims, device=dev, separate_y=False if w.x_dtype == w.y_dtype else None)
+    stream = torch.cuda.current_stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    def step(ev):
+        ev[0].record(stream)
+        moe.route_topk(dims, inp.logits, inp.bias, w.score_fn, w.renormalize, b.topk_idx,
+                       b.topk_w, stream)
+        ev[1].record(stream)
+        moe.dispatch_count(dims, b.topk_idx, b.expert_counts, b.expert_offsets, b.rank_counts,
+                           b.rank_offsets, b.send_counts, b.pos, b.status, stream)
+        ev[2].record(stream)
+        moe.dispatch_pack(dims, inp.x, inp.x_scales, b.pos, b.packed_x, b.packed_scales,
+                          b.packed_src, stream)
+        ev[3].record(stream)
+        flush()  # expert-op stand-in: nothing survives in L2 between pack and combine
+        ev[4].record(stream)
+        moe.combine(dims, b.y, b.pos, b.topk_w, b.out, stream)
+        ev[5].record(stream)
+
+    def new_events():
+        return [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+
+    for _ in range(max(3, args.warmup)):
+        flush()
+        step(new_events())
+    st = moe.read_status(b.status, stream)
+    if st != moe.MOE_OK:
+        raise SystemExit(f"dispatch_count status {moe.STATUS_NAMES.get(st, st)} on {w.name}")
+
+    sampler = None if args.no_clocks else ClockSampler(local_rank)
+    if sampler is not None:
+        sampler.wait_first()
+    evs = [new_events() for _ in range(args.steps)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        flush()
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    t_wall1 = time.time()
+    clocks = None
+    if sampler is not None:
+        time.sleep(0.05)
+        sampler.stop()
+        clocks = sampler.summary(t_wall0, t_wall1)
+
+    per = {k: [] for k in KERNELS}
+    for ev in evs:
+        per["route"].append(ev[0].elapsed_time(ev[1]))
+        per["count"].append(ev[1].elapsed_time(ev[2]))
+        per["pack"].append(ev[2].elapsed_time(ev[3]))
+        per["combine"].append(ev[4].elapsed_time(ev[5]))
+    step_ms = [sum(per[k][i] for k in KERNELS) for i in range(args.steps)]
+    ms = statistics.mean(step_ms)
+    if pg:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * w.NT / (ms / 1e3)
+
+    # ---- end to end through the public API with host buffers -------------
+    e2e = run_e2e(args, w, dims, inp_cpu, b, dev, stream, flush, moe)
+
+    alg = W.algorithmic_bytes(w)
+    peak, peak_kind = measured_peaks()
+    kern = {}
+    for k in KERNELS:
+        mean_ms = statistics.mean(per[k])
+        kern[k] = {"ms": mean_ms, "median_ms": statistics.median(per[k]),
+                   "alg_bytes": alg[k], "alg_gbs": alg[k] / (mean_ms / 1e3) / 1e9}
+    dom = max(("pack", "combine"), key=lambda k: kern[k]["ms"])
+    achieved = kern[dom]["alg_gbs"]
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s",
+                "unit": "GB/s", "frac": achieved / peak, "traffic": ncu_traffic(dom, w.name)}
+    pc_ms = kern["pack"]["ms"] + kern["combine"]["ms"]
+    pc_gbs = (alg["pack"] + alg["combine"]) / (pc_ms / 1e3) / 1e9
+
+    if rank != 0:
+        return 0
+    cpu = None
+    if world == 1 and args.cpu_seconds > 0:
+        import oracle
+        oracle.build_lib()
+        cpu = cpu_baseline(w, inp_cpu, args.cpu_seconds)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "io_dtype": "bf16", "data": "synthetic", "config": workload_config(w),
+        "gpu_launches": 4 * args.steps,
+        "roofline": roofline,
+        "pack_plus_combine": {"ms": pc_ms, "alg_gbs": pc_gbs, "frac": pc_gbs / peak,
+                              "frac_of_8tbs_nominal": pc_gbs / 8000.0},
+        "kernels": kern,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "wall_s_timed_region": t_wall1 - t_wall0,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_e2e(args, w, dims, inp_cpu, b, dev, stream, flush, moe):
+    """Same path through the public API, inputs copied from pinned host
+    memory and the combined output copied back inside the timed region."""
+    import torch
+    h_logits = inp_cpu.logits.pin_memory()
+    h_bias = None if inp_cpu.bias is None else inp_cpu.bias.pin_memory()
+    h_x = inp_cpu.x.pin_memory()
+    h_xs = None if inp_cpu.x_scales is None else inp_cpu.x_scales.pin_memory()
+    h_out = torch.empty(b.out.shape, dtype=b.out.dtype).pin_memory()
+    d_logits = torch.empty_like(h_logits, device=dev)
+    d_bias = None if h_bias is None else torch.empty_like(h_bias, device=dev)
+    d_x = torch.empty_like(h_x, device=dev)
+    d_xs = None if h_xs is None else torch.empty_like(h_xs, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in (h_logits, h_bias, h_x, h_xs) if t is not None)
+    d2h = h_out.numel() * h_out.element_size()
+
+    def one(e0, e1):
+        e0.record(stream)
+        d_logits.copy_(h_logits, non_blocking=True)
+        if d_bias is not None:
+            d_bias.copy_(h_bias, non_blocking=True)
+        d_x.copy_(h_x, non_blocking=True)
+        if d_xs is not None:
+            d_xs.copy_(h_xs, non_blocking=True)
+        moe.route_topk(dims, d_logits, d_bias, w.score_fn, w.renormalize, b.topk_idx, b.topk_w,
+                       stream)
+        moe.dispatch_count(dims, b.topk_idx, b.expert_counts, b.expert_offsets, b.rank_counts,
+                           b.rank_offsets, b.send_counts, b.pos, b.status, stream)
+        moe.dispatch_pack(dims, d_x, d_xs, b.pos, b.packed_x, b.packed_scales, b.packed_src,
+                          stream)
+        moe.combine(dims, b.y, b.pos, b.topk_w, b.out, stream)
+        h_out.copy_(b.out, non_blocking=True)
+        e1.record(stream)
+
+    n = max(1, args.e2e_steps)
+    for _ in range(3):
+        flush()
+        one(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    torch.cuda.synchronize(dev)
+    for e0, e1 in evs:
+        flush()
+        one(e0, e1)
+    torch.cuda.synchronize(dev)
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+    return {"value": w.NT / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,234 @@
+// C entry points of libmoe_route.so: argument validation on the host, then
+// one launcher per step.  See include/moe_route.h for the contract.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+thread_local char g_err[512] = "";
+}
+
+int set_error(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int sm_count() {
+    static thread_local int dev_cached = -1, sms = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev != dev_cached) {
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 0;
+        dev_cached = dev;
+    }
+    return sms;
+}
+
+namespace {
+
+constexpr int64_t kI32Max = 2147483647;
+
+struct Derived {
+    int64_t NT, cap, rows_total, pairs, x_row_bytes, y_row_bytes;
+    int scales_per_row;
+};
+
+int elem_bytes(int dtype) {
+    switch (dtype) {
+        case MOE_BF16: return 2;
+        case MOE_F32: return 4;
+        case MOE_FP8E4M3_BLK128: return 1;
+        default: return 0;
+    }
+}
+
+// Validates dims and fills the derived sizes.  `what` names the caller.
+int check_dims(const MoeDims *d, Derived *out, const char *what) {
+    g_err[0] = '\0';
+    if (d == nullptr) return set_error(MOE_ERR_INVALID_ARG, "%s: dims is NULL", what);
+    if (d->N < 1 || d->T < 0 || d->E < 1 || d->R < 1 || d->H < 1)
+        return set_error(MOE_ERR_INVALID_ARG, "%s: need N>=1, T>=0, E>=1, R>=1, H>=1 (got N=%d T=%d E=%d R=%d H=%d)",
+                         what, d->N, d->T, d->E, d->R, d->H);
+    if (d->E % d->N != 0)
+        return set_error(MOE_ERR_INVALID_ARG, "%s: E=%d is not a multiple of N=%d", what, d->E, d->N);
+    if (d->R > d->E)
+        return set_error(MOE_ERR_INVALID_ARG, "%s: R=%d exceeds E=%d", what, d->R, d->E);
+    if (d->E > 1024 || d->R > 32)
+        return set_error(MOE_ERR_UNSUPPORTED, "%s: this build supports E<=1024 and R<=32 (got E=%d R=%d)",
+                         what, d->E, d->R);
+    if (d->reserved != 0) return set_error(MOE_ERR_INVALID_ARG, "%s: dims.reserved must be 0", what);
+    if (elem_bytes(d->x_dtype) == 0)
+        return set_error(MOE_ERR_INVALID_ARG, "%s: unknown x_dtype %d", what, d->x_dtype);
+    if (d->y_dtype != MOE_BF16 && d->y_dtype != MOE_F32)
+        return set_error(MOE_ERR_INVALID_ARG, "%s: y_dtype must be MOE_BF16 or MOE_F32 (got %d)", what,
+                         d->y_dtype);
+    if (d->H % 8 != 0)
+        return set_error(MOE_ERR_INVALID_ARG, "%s: H=%d must be a multiple of 8", what, d->H);
+    if (d->x_dtype == MOE_FP8E4M3_BLK128 && d->H % 128 != 0)
+        return set_error(MOE_ERR_INVALID_ARG, "%s: fp8 rows need H %% 128 == 0 (got H=%d)", what, d->H);
+    if (d->cap_rows < 0) return set_error(MOE_ERR_INVALID_ARG, "%s: cap_rows < 0", what);
+    Derived v;
+    v.NT = (int64_t)d->N * d->T;
+    const int64_t L = d->E / d->N;
+    const int64_t bound = v.NT * (d->R > L ? d->R : L);
+    v.cap = d->cap_rows > 0 ? d->cap_rows : bound;
+    if (v.cap < 1) v.cap = 1;  // T == 0: keep the region arithmetic well defined
+    v.pairs = v.NT * d->R;
+    v.rows_total = (int64_t)d->N * v.cap;
+    if (v.pairs > kI32Max || v.rows_total > kI32Max)
+        return set_error(MOE_ERR_UNSUPPORTED,
+                         "%s: N*T*R=%lld and N*cap=%lld must stay below 2^31 (32-bit row indices)",
+                         what, (long long)v.pairs, (long long)v.rows_total);
+    v.x_row_bytes = (int64_t)d->H * elem_bytes(d->x_dtype);
+    v.y_row_bytes = (int64_t)d->H * elem_bytes(d->y_dtype);
+    v.scales_per_row = d->x_dtype == MOE_FP8E4M3_BLK128 ? d->H / 128 : 0;
+    if (out) *out = v;
+    return MOE_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int cuda_result(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return MOE_OK;
+    return set_error(MOE_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_version(void) { return 10000; }
+
+const char *moe_last_error(void) { return g_err; }
+
+int moe_buffer_sizes(const MoeDims *dims, MoeSizes *out) {
+    Derived v;
+    int rc = check_dims(dims, &v, "moe_buffer_sizes");
+    if (rc != MOE_OK) return rc;
+    if (out == nullptr) return set_error(MOE_ERR_INVALID_ARG, "moe_buffer_sizes: out is NULL");
+    const int64_t N = dims->N, E = dims->E, H = dims->H;
+    const int64_t L = E / N;
+    memset(out, 0, sizeof(*out));
+    out->bound_rows = v.NT * (dims->R > L ? dims->R : L);
+    out->cap_rows = v.cap;
+    out->total_pairs = v.pairs;
+    out->logits_bytes = v.NT * E * 4;
+    out->topk_idx_bytes = v.pairs * 4;
+    out->topk_w_bytes = v.pairs * 4;
+    out->pos_bytes = v.pairs * 4;
+    out->expert_counts_bytes = E * 4;
+    out->expert_offsets_bytes = (E + 1) * 4;
+    out->rank_counts_bytes = N * 4;
+    out->rank_offsets_bytes = (N + 1) * 4;
+    out->send_counts_bytes = N * N * 4;
+    out->x_bytes = v.NT * v.x_row_bytes;
+    out->x_scales_bytes = v.NT * v.scales_per_row * 4;
+    out->packed_x_bytes = v.rows_total * v.x_row_bytes;
+    out->packed_scales_bytes = v.rows_total * v.scales_per_row * 4;
+    out->packed_src_bytes = v.rows_total * 4;
+    out->y_bytes = v.rows_total * v.y_row_bytes;
+    out->out_bytes = v.NT * v.y_row_bytes;
+    out->status_bytes = 4;
+    (void)H;
+    return MOE_OK;
+}
+
+int moe_route_topk(const MoeDims *dims, const float *logits, const float *bias, int score_fn,
+                   int renormalize, int32_t *topk_idx, float *topk_w, void *stream) {
+    Derived v;
+    int rc = check_dims(dims, &v, "moe_route_topk");
+    if (rc != MOE_OK) return rc;
+    if (score_fn != MOE_SOFTMAX && score_fn != MOE_SIGMOID)
+        return set_error(MOE_ERR_INVALID_ARG, "moe_route_topk: unknown score_fn %d", score_fn);
+    if (v.NT == 0) return MOE_OK;
+    if (!logits || !topk_idx || !topk_w)
+        return set_error(MOE_ERR_INVALID_ARG, "moe_route_topk: logits, topk_idx and topk_w must be non-NULL");
+    if (!aligned(logits, 4) || !aligned(topk_idx, 4) || !aligned(topk_w, 4) || (bias && !aligned(bias, 4)))
+        return set_error(MOE_ERR_INVALID_ARG, "moe_route_topk: pointers must be 4-byte aligned");
+    return cuda_result(launch_route_topk(logits, bias, v.NT, dims->E, dims->R, score_fn, renormalize ? 1 : 0,
+                                         topk_idx, topk_w, (cudaStream_t)stream),
+                       "moe_route_topk");
+}
+
+int moe_dispatch_count(const MoeDims *dims, const int32_t *topk_idx, int32_t *expert_counts,
+                       int32_t *expert_offsets, int32_t *rank_counts, int32_t *rank_offsets,
+                       int32_t *send_counts, int32_t *pos, int32_t *status, void *stream) {
+    Derived v;
+    int rc = check_dims(dims, &v, "moe_dispatch_count");
+    if (rc != MOE_OK) return rc;
+    if (!expert_counts || !expert_offsets || !rank_counts || !rank_offsets || !send_counts || !status ||
+        (v.NT > 0 && (!topk_idx || !pos)))
+        return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_count: a required pointer is NULL");
+    const void *ptrs[] = {topk_idx, expert_counts, expert_offsets, rank_counts, rank_offsets,
+                          send_counts, pos, status};
+    for (const void *p : ptrs)
+        if (p && !aligned(p, 4))
+            return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_count: pointers must be 4-byte aligned");
+    cudaError_t e = launch_dispatch_count(topk_idx, dims->N, dims->T, dims->E, dims->R, v.cap,
+                                          expert_counts, expert_offsets, rank_counts, rank_offsets,
+                                          send_counts, pos, status, (cudaStream_t)stream);
+    if (e == cudaErrorNotSupported)
+        return set_error(MOE_ERR_UNSUPPORTED,
+                         "moe_dispatch_count: the device cannot schedule a thread-block cluster of this kernel");
+    return cuda_result(e, "moe_dispatch_count");
+}
+
+int moe_dispatch_pack(const MoeDims *dims, const void *x, const float *x_scales, const int32_t *pos,
+                      void *packed_x, float *packed_scales, int32_t *packed_src, void *stream) {
+    Derived v;
+    int rc = check_dims(dims, &v, "moe_dispatch_pack");
+    if (rc != MOE_OK) return rc;
+    if (v.NT == 0) return MOE_OK;
+    const bool fp8 = dims->x_dtype == MOE_FP8E4M3_BLK128;
+    if (!x || !pos || !packed_x || !packed_src || (fp8 && (!x_scales || !packed_scales)))
+        return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_pack: a required pointer is NULL");
+    if (!aligned(x, 16) || !aligned(packed_x, 16))
+        return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_pack: x and packed_x must be 16-byte aligned");
+    if (!aligned(pos, 4) || !aligned(packed_src, 4) || (fp8 && (!aligned(x_scales, 4) || !aligned(packed_scales, 4))))
+        return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_pack: index and scale pointers must be 4-byte aligned");
+    return cuda_result(launch_dispatch_pack(x, fp8 ? x_scales : nullptr, pos, v.NT, dims->R, v.x_row_bytes,
+                                            v.scales_per_row, v.rows_total, packed_x,
+                                            fp8 ? packed_scales : nullptr, packed_src,
+                                            (cudaStream_t)stream),
+                       "moe_dispatch_pack");
+}
+
+int moe_combine(const MoeDims *dims, const void *y, const int32_t *pos, const float *topk_w, void *out,
+                void *stream) {
+    Derived v;
+    int rc = check_dims(dims, &v, "moe_combine");
+    if (rc != MOE_OK) return rc;
+    if (v.NT == 0) return MOE_OK;
+    if (!y || !pos || !topk_w || !out)
+        return set_error(MOE_ERR_INVALID_ARG, "moe_combine: a required pointer is NULL");
+    if (!aligned(y, 16) || !aligned(out, 16))
+        return set_error(MOE_ERR_INVALID_ARG, "moe_combine: y and out must be 16-byte aligned");
+    if (!aligned(pos, 4) || !aligned(topk_w, 4))
+        return set_error(MOE_ERR_INVALID_ARG, "moe_combine: pos and topk_w must be 4-byte aligned");
+    return cuda_result(launch_combine(y, dims->y_dtype, pos, topk_w, v.NT, dims->R, dims->H, v.rows_total,
+                                      out, (cudaStream_t)stream),
+                       "moe_combine");
+}
+
+int moe_read_status(const int32_t *status, void *stream) {
+    g_err[0] = '\0';
+    if (!status) return set_error(MOE_ERR_INVALID_ARG, "moe_read_status: status is NULL");
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_result(e, "moe_read_status");
+    int32_t host = 0;
+    e = cudaMemcpy(&host, status, sizeof(host), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_result(e, "moe_read_status");
+    return host;
+}
+
+}  // extern "C"

@@ -1,0 +1,39 @@
+// Internal declarations shared by the translation units of libmoe_route.so.
+// Not part of the public ABI (that is include/moe_route.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_route.h"
+
+namespace moe {
+
+// Sets the calling thread's message for moe_last_error(); returns `code`.
+int set_error(int code, const char *fmt, ...);
+
+// Multiprocessor count of the current device (cached per device).
+int sm_count();
+
+// ---- launchers (arguments already validated by the C entry points) -------
+
+cudaError_t launch_route_topk(const float *logits, const float *bias, int64_t NT, int E, int R,
+                              int score_fn, int renormalize, int32_t *topk_idx, float *topk_w,
+                              cudaStream_t stream);
+
+cudaError_t launch_dispatch_count(const int32_t *topk_idx, int N, int T, int E, int R,
+                                  int64_t cap, int32_t *expert_counts, int32_t *expert_offsets,
+                                  int32_t *rank_counts, int32_t *rank_offsets,
+                                  int32_t *send_counts, int32_t *pos, int32_t *status,
+                                  cudaStream_t stream);
+
+cudaError_t launch_dispatch_pack(const void *x, const float *x_scales, const int32_t *pos,
+                                 int64_t NT, int R, int64_t row_bytes, int scales_per_row,
+                                 int64_t rows_total, void *packed_x, float *packed_scales,
+                                 int32_t *packed_src, cudaStream_t stream);
+
+cudaError_t launch_combine(const void *y, int y_dtype, const int32_t *pos, const float *topk_w,
+                           int64_t NT, int R, int H, int64_t rows_total, void *out,
+                           cudaStream_t stream);
+
+}  // namespace moe

@@ -1,0 +1,171 @@
+// Route top-k: one warp per token.
+//
+// "Efficient and portable mixture-of-experts communication", section
+// "Introduction": a small linear router produces a probability distribution
+// over the experts; each token goes to its top-K experts, weighted by it.
+// "Lower latency and higher throughput with multi-node DeepSeek
+// deployment", section "MoE Router": the pages do this with a sort that
+// carries the element indices.  Here a full sort is unnecessary: R rounds of
+// a warp-wide arg-max select the same experts in the same order.
+//
+// Layout: lane l owns the J consecutive experts [l*J, l*J + J), J a
+// compile-time constant with 32*J >= E.  Because lower lanes own lower
+// expert ids, "highest key, then lowest lane, then lowest slot" is exactly
+// "highest z, then lowest expert index" -- the tie rule of the definition.
+#include <math.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kRouteThreads = 256;  // 8 tokens per block
+
+template <int J>
+__device__ __forceinline__ void local_best(const float (&z)[J], uint32_t live, float &v, int &jb) {
+    v = -INFINITY;
+    jb = -1;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        if ((live >> j) & 1u) {
+            if (jb < 0 || z[j] > v) {  // strict '>' keeps the lowest slot on ties
+                v = z[j];
+                jb = j;
+            }
+        }
+    }
+}
+
+template <int J, bool kVec4>
+__global__ void __launch_bounds__(kRouteThreads)
+route_topk_kernel(const float *__restrict__ logits, const float *__restrict__ bias, int64_t NT,
+                  int E, int R, int score_fn, int renormalize, int32_t *__restrict__ topk_idx,
+                  float *__restrict__ topk_w) {
+    const int lane = threadIdx.x & 31;
+    const int64_t g = (int64_t)blockIdx.x * (kRouteThreads / 32) + (threadIdx.x >> 5);
+    if (g >= NT) return;  // uniform per warp
+
+    const float *row = logits + g * E;
+    const int e0 = lane * J;
+    float z[J];
+    uint32_t valid = 0;
+#pragma unroll
+    for (int j = 0; j < J; ++j) z[j] = -INFINITY;
+    if (kVec4) {
+        // E % 4 == 0 and J % 4 == 0: e0 + j is a multiple of 4, so the
+        // 16-byte load is aligned and stays inside the row.
+#pragma unroll
+        for (int j = 0; j < J; j += 4) {
+            if (e0 + j < E) {
+                float4 v = __ldg(reinterpret_cast<const float4 *>(row + e0 + j));
+                z[j] = v.x;
+                z[j + 1] = v.y;
+                z[j + 2] = v.z;
+                z[j + 3] = v.w;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < J; ++j)
+            if (e0 + j < E) z[j] = __ldg(row + e0 + j);
+    }
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        if (e0 + j < E) {
+            valid |= 1u << j;
+            if (bias != nullptr) z[j] = __fadd_rn(z[j], __ldg(bias + e0 + j));
+        }
+    }
+
+    // R rounds of warp arg-max.  Each lane keeps its own best live slot and
+    // only the winning lane rescans after a round.
+    uint32_t live = valid;
+    float v;
+    int jb;
+    local_best<J>(z, live, v, jb);
+    float zmax = 0.f;
+    int my_e = 0;
+    float my_z = 0.f;
+    for (int k = 0; k < R; ++k) {
+        float vmax = v;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, off));
+        unsigned ball = __ballot_sync(kFull, jb >= 0 && v == vmax);
+        if (ball == 0u) ball = __ballot_sync(kFull, jb >= 0);  // only with NaN keys
+        const int wl = __ffs(ball) - 1;
+        const int wj = __shfl_sync(kFull, jb, wl);
+        const float wz = __shfl_sync(kFull, v, wl);
+        if (k == 0) zmax = wz;
+        if (lane == k) {
+            my_e = wl * J + wj;
+            my_z = wz;
+        }
+        if (lane == wl) {
+            live &= ~(1u << wj);
+            local_best<J>(z, live, v, jb);
+        }
+    }
+
+    float p = 0.f;
+    if (score_fn == MOE_SOFTMAX) {
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < J; ++j)
+            if ((valid >> j) & 1u) s += expf(z[j] - zmax);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
+        if (lane < R) p = expf(my_z - zmax) / s;
+    } else {
+        if (lane < R) p = 1.0f / (1.0f + expf(-my_z));
+    }
+    if (renormalize) {
+        float t = p;  // lanes >= R hold 0
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(kFull, t, off);
+        p = p / t;
+    }
+    if (lane < R) {
+        topk_idx[g * R + lane] = my_e;
+        topk_w[g * R + lane] = p;
+    }
+}
+
+template <int J>
+cudaError_t launch_j(const float *logits, const float *bias, int64_t NT, int E, int R, int score_fn,
+                     int renormalize, int32_t *topk_idx, float *topk_w, cudaStream_t stream) {
+    const int64_t blocks = (NT + kRouteThreads / 32 - 1) / (kRouteThreads / 32);
+    const bool vec4 = (J % 4 == 0) && (E % 4 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15) == 0);
+    if (vec4) {
+        if constexpr (J % 4 == 0)
+            route_topk_kernel<J, true><<<(unsigned)blocks, kRouteThreads, 0, stream>>>(
+                logits, bias, NT, E, R, score_fn, renormalize, topk_idx, topk_w);
+    } else {
+        route_topk_kernel<J, false><<<(unsigned)blocks, kRouteThreads, 0, stream>>>(
+            logits, bias, NT, E, R, score_fn, renormalize, topk_idx, topk_w);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_route_topk(const float *logits, const float *bias, int64_t NT, int E, int R,
+                              int score_fn, int renormalize, int32_t *topk_idx, float *topk_w,
+                              cudaStream_t stream) {
+    if (NT == 0) return cudaSuccess;
+    const int need = (E + 31) / 32;  // slots per lane
+#define MOE_ROUTE_CASE(JV) \
+    if (need <= JV) return launch_j<JV>(logits, bias, NT, E, R, score_fn, renormalize, topk_idx, topk_w, stream);
+    MOE_ROUTE_CASE(1)
+    MOE_ROUTE_CASE(2)
+    MOE_ROUTE_CASE(4)
+    MOE_ROUTE_CASE(8)
+    MOE_ROUTE_CASE(12)
+    MOE_ROUTE_CASE(16)
+    MOE_ROUTE_CASE(24)
+    MOE_ROUTE_CASE(32)
+#undef MOE_ROUTE_CASE
+    return cudaErrorInvalidValue;  // E > 1024 is rejected before this point
+}
+
+}  // namespace moe

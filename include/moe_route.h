@@ -1,0 +1,188 @@
+/*
+ * moe_route.h -- C ABI of the GB300 (sm_103a) MoE token-routing library
+ * (libmoe_route.so): route top-k, dispatch count, dispatch pack, combine.
+ *
+ * The routing problem follows "Enabling trillion-parameter models on AWS
+ * EFA", section "Send and receive buffers": N ranks, T tokens per rank, each
+ * token routed to R of E experts, hidden size H; one rank receives at most
+ * N*T*max(R, E/N) rows.  Here all N ranks are partitions of one GPU's memory:
+ * rank d owns experts [d*E/N, (d+1)*E/N) and a receive region of cap_rows
+ * rows; a "send" is a store into another rank's region.
+ *
+ * Conventions for every entry point:
+ *   - All array pointers are DEVICE pointers owned by the caller; the library
+ *     allocates nothing and keeps no pointer after the call returns.
+ *   - Arrays are dense and row-major; token g = s*T + t is token t of source
+ *     rank s.  Rows of x, packed_x, y and out must start on 16-byte
+ *     boundaries (H as required below guarantees it when the base is).
+ *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is
+ *     the legacy default stream).  No call synchronises the host except
+ *     moe_read_status.  Grids depend only on the dimensions, never on
+ *     routing results, so a call sequence can be captured in a CUDA graph.
+ *   - Return value: MOE_OK, or a negative MOE_ERR_* code.  Argument errors
+ *     are detected on the host before anything is enqueued; the message is
+ *     available from moe_last_error() in the calling thread.
+ *   - Device-side problems (a rank over capacity, invalid expert ids) never
+ *     trap: moe_dispatch_count writes a status word on the device, pos
+ *     entries of affected pairs become -1, and later steps skip them.
+ */
+#ifndef MOE_ROUTE_H
+#define MOE_ROUTE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1) /* bad dims/pointers; also device status for invalid expert ids */
+#define MOE_ERR_UNSUPPORTED (-2) /* valid request this build does not implement */
+#define MOE_ERR_CUDA (-3)        /* a CUDA runtime call or kernel launch failed */
+#define MOE_ERR_CAPACITY (-4)    /* device status: a rank received more than cap_rows rows */
+#define MOE_ERR_TIMEOUT (-5)     /* device status: a bounded wait gave up */
+
+/* ---- element types ------------------------------------------------------ */
+#define MOE_BF16 0           /* bfloat16 */
+#define MOE_F32 1            /* IEEE binary32 */
+#define MOE_FP8E4M3_BLK128 2 /* fp8 e4m3 codes + one f32 scale per 128 elements (x only) */
+
+/* ---- router score functions --------------------------------------------- */
+#define MOE_SOFTMAX 0 /* softmax over all E experts, then top-R */
+#define MOE_SIGMOID 1 /* logistic sigmoid per expert */
+
+/* Problem dimensions.  Limits: N >= 1, T >= 0, 1 <= E <= 1024, E % N == 0,
+ * 1 <= R <= min(E, 32), H >= 8 and H % 8 == 0 (H % 128 == 0 for fp8 x),
+ * N*T*R < 2^31, N*cap_rows < 2^31. */
+typedef struct MoeDims {
+    int32_t N;        /* ranks (partitions of one GPU's memory) */
+    int32_t T;        /* tokens per rank */
+    int32_t E;        /* experts; expert e lives on rank e / (E/N) */
+    int32_t R;        /* experts per token */
+    int32_t H;        /* hidden size (elements per token row) */
+    int32_t x_dtype;  /* MOE_BF16, MOE_F32 or MOE_FP8E4M3_BLK128: dispatched rows */
+    int32_t y_dtype;  /* MOE_BF16 or MOE_F32: expert outputs read by combine and its output */
+    int32_t reserved; /* must be 0 */
+    int64_t cap_rows; /* rows per rank receive region; 0 selects N*T*max(R, E/N) */
+} MoeDims;
+
+/* Sizes of every buffer the caller allocates, in bytes (moe_buffer_sizes). */
+typedef struct MoeSizes {
+    int64_t bound_rows;          /* N*T*max(R, E/N): the pages' worst case per rank */
+    int64_t cap_rows;            /* effective per-rank capacity */
+    int64_t total_pairs;         /* N*T*R routed (token, expert) pairs */
+    int64_t logits_bytes;        /* f32 [N*T][E] */
+    int64_t topk_idx_bytes;      /* i32 [N*T][R] */
+    int64_t topk_w_bytes;        /* f32 [N*T][R] */
+    int64_t pos_bytes;           /* i32 [N*T][R] */
+    int64_t expert_counts_bytes; /* i32 [E] */
+    int64_t expert_offsets_bytes;/* i32 [E+1] */
+    int64_t rank_counts_bytes;   /* i32 [N] */
+    int64_t rank_offsets_bytes;  /* i32 [N+1] */
+    int64_t send_counts_bytes;   /* i32 [N][N] */
+    int64_t x_bytes;             /* [N*T][H] of x_dtype */
+    int64_t x_scales_bytes;      /* f32 [N*T][H/128] (fp8 only, else 0) */
+    int64_t packed_x_bytes;      /* [N*cap][H] of x_dtype */
+    int64_t packed_scales_bytes; /* f32 [N*cap][H/128] (fp8 only, else 0) */
+    int64_t packed_src_bytes;    /* i32 [N*cap] */
+    int64_t y_bytes;             /* [N*cap][H] of y_dtype */
+    int64_t out_bytes;           /* [N*T][H] of y_dtype */
+    int64_t status_bytes;        /* i32 [1] */
+} MoeSizes;
+
+/* Fill *out with the buffer sizes for dims (host only, no CUDA call).
+ * Returns MOE_OK or MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED. */
+int moe_buffer_sizes(const MoeDims *dims, MoeSizes *out);
+
+/* Route top-k.  Source: "Efficient and portable mixture-of-experts
+ * communication", section "Introduction" (a small linear router yields a
+ * probability distribution; the top-K experts are chosen and weighted by
+ * it); "Lower latency and higher throughput with multi-node DeepSeek
+ * deployment", section "MoE Router" (top-k with index tracking; one router
+ * serves DeepSeek- and Mixtral-style models).
+ *   logits   f32 [N*T][E]            router logits
+ *   bias     f32 [E] or NULL         per-expert bias added to every logit
+ *   score_fn MOE_SOFTMAX | MOE_SIGMOID
+ *   renormalize  nonzero: divide the selected scores by their sum
+ *   topk_idx i32 [N*T][R] (out)      experts by key z = fl32(logit + bias)
+ *                                    descending; equal keys -> lower index
+ *   topk_w   f32 [N*T][R] (out)      score of each selected expert
+ * Scores are computed from z in f32 (softmax over all E).  Non-finite logits
+ * give unspecified, but always in-range, selections. */
+int moe_route_topk(const MoeDims *dims, const float *logits, const float *bias, int score_fn,
+                   int renormalize, int32_t *topk_idx, float *topk_w, void *stream);
+
+/* Dispatch count.  Source: "Enabling trillion-parameter models on AWS EFA",
+ * section "Dispatch and combine" (per-expert token counts from
+ * shared-memory atomics, then a cumulative sum gives the offsets for
+ * packing tokens contiguously per destination); "Efficient and portable
+ * mixture-of-experts communication", section "Dispatch" (tokens grouped per
+ * expert for the grouped GEMM).
+ *   topk_idx       i32 [N*T][R] (in)
+ *   expert_counts  i32 [E]   (out) pairs routed to each expert
+ *   expert_offsets i32 [E+1] (out) exclusive prefix sum of expert_counts
+ *   rank_counts    i32 [N]   (out) rows each rank receives (may exceed cap)
+ *   rank_offsets   i32 [N+1] (out) exclusive prefix sum of rank_counts
+ *   send_counts    i32 [N][N](out) [s][d]: rows source rank s sends to rank d
+ *   pos            i32 [N*T][R] (out) receive row of pair (g,k):
+ *                  d*cap + (expert_offsets[e] - rank_offsets[d]) + (number of
+ *                  earlier tokens routed to e); -1 for a dropped pair
+ *   status         i32 [1]   (out, device) MOE_OK, MOE_ERR_CAPACITY (some
+ *                  rank over cap; its last rows get pos = -1) or
+ *                  MOE_ERR_INVALID_ARG (an expert id outside [0,E) or a
+ *                  repeated expert within a token; those pairs get pos = -1
+ *                  and are not counted)
+ * Within a rank region rows are grouped by expert (ascending) and ordered
+ * by token (ascending) inside an expert: deterministic, independent of
+ * scheduling.  Read status with moe_read_status. */
+int moe_dispatch_count(const MoeDims *dims, const int32_t *topk_idx, int32_t *expert_counts,
+                       int32_t *expert_offsets, int32_t *rank_counts, int32_t *rank_offsets,
+                       int32_t *send_counts, int32_t *pos, int32_t *status, void *stream);
+
+/* Dispatch pack.  Source: "Efficient and portable mixture-of-experts
+ * communication", section "Dispatch" (the message of a token is its
+ * activations, their block scales and its index on the source rank);
+ * "Enabling trillion-parameter models on AWS EFA", section "Dispatch and
+ * combine" (tokens packed contiguously per destination).
+ *   x             [N*T][H] of x_dtype (in)
+ *   x_scales      f32 [N*T][H/128] (in, fp8 only; else NULL)
+ *   pos           i32 [N*T][R] from moe_dispatch_count
+ *   packed_x      [N*cap][H] of x_dtype (out): row pos[g][k] = x[g]
+ *   packed_scales f32 [N*cap][H/128] (out, fp8 only; else NULL)
+ *   packed_src    i32 [N*cap] (out): row pos[g][k] = g*R + k
+ * Only rows [d*cap, d*cap + min(rank_counts[d], cap)) of each region are
+ * written; pairs with pos < 0 (or outside [0, N*cap)) are skipped. */
+int moe_dispatch_pack(const MoeDims *dims, const void *x, const float *x_scales,
+                      const int32_t *pos, void *packed_x, float *packed_scales,
+                      int32_t *packed_src, void *stream);
+
+/* Combine.  Source: "Efficient and portable mixture-of-experts
+ * communication", section "Combine" (each token reads its experts' outputs
+ * through the routing table and forms their router-weighted average);
+ * "Enabling trillion-parameter models on AWS EFA", sections "Dispatch and
+ * combine" and "Evaluation" (accumulation on the receiving side only).
+ *   y      [N*cap][H] of y_dtype (in): expert output of each received row
+ *   pos    i32 [N*T][R], topk_w f32 [N*T][R] (in)
+ *   out    [N*T][H] of y_dtype (out): out[g] = sum_k topk_w[g][k] * y[pos[g][k]],
+ *          accumulated in f32 in k order, rounded once (bf16: to nearest even).
+ * Pairs with pos < 0 (or outside [0, N*cap)) contribute nothing. */
+int moe_combine(const MoeDims *dims, const void *y, const int32_t *pos, const float *topk_w,
+                void *out, void *stream);
+
+/* Wait for `stream`, then read the device status word written by
+ * moe_dispatch_count.  Returns that status (MOE_OK or a MOE_ERR_* code), or
+ * MOE_ERR_CUDA if the wait or the copy failed. */
+int moe_read_status(const int32_t *status, void *stream);
+
+/* Message for the last error returned in the calling thread ("" if none). */
+const char *moe_last_error(void);
+
+/* Library ABI version (major*10000 + minor*100 + patch). */
+int moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_ROUTE_H */

@@ -278,6 +278,8 @@ int oracle_expert_op(int op /*0 identity, 1 scale, 2 dequant*/, int64_t rows, in
                      int x_dtype, int y_dtype, const uint8_t *packed_x,
                      const float *packed_scales, const int32_t *packed_src,
                      const int32_t *topk_idx, void *y) {
+    float fp8_value[256]; /* every e4m3 code decoded once (exact in float) */
+    for (int b = 0; b < 256; ++b) fp8_value[b] = (float)fp8e4m3_to_double((uint8_t)b);
     for (int64_t c = 0; c < rows; ++c) {
         if (packed_src[c] < 0) continue;
         int e = topk_idx[packed_src[c]];
@@ -286,7 +288,7 @@ int oracle_expert_op(int op /*0 identity, 1 scale, 2 dequant*/, int64_t rows, in
             float v;
             if (x_dtype == OR_BF16) v = bf16_to_f32(((const uint16_t *)packed_x)[c * H + h]);
             else if (x_dtype == OR_F32) v = ((const float *)packed_x)[c * H + h];
-            else v = (float)fp8e4m3_to_double(packed_x[c * H + h]);
+            else v = fp8_value[packed_x[c * H + h]];
             if (op == 1) v = v * s;
             else if (op == 2) v = v * packed_scales[c * (H / 128) + h / 128];
             if (y_dtype == OR_BF16) ((uint16_t *)y)[c * H + h] = f32_to_bf16(v);

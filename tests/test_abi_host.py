@@ -1,0 +1,139 @@
+"""Host-side checks of the C ABI: the library builds for sm_103a, loads,
+exports every entry point the header declares, sizes buffers, and rejects bad
+arguments before touching the GPU.  No kernel is launched here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import combine_moe_route_topk_gb300 as moe
+from combine_moe_route_topk_gb300 import _build
+from combine_moe_route_topk_gb300 import workloads as W
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return moe.lib()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "moe_route.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("moe_buffer_sizes", "moe_route_topk", "moe_dispatch_count", "moe_dispatch_pack",
+              "moe_combine", "moe_read_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_is_built_for_sm_103a_only():
+    assert _build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_version(lib):
+    assert lib.moe_version() == 10000
+
+
+@pytest.mark.parametrize("name", list(W.WORKLOADS))
+def test_buffer_sizes_follow_the_bound(lib, name):
+    w = W.WORKLOADS[name]
+    s = moe.buffer_sizes(moe.dims_of(w))
+    L = w.E // w.N
+    bound = w.N * w.T * max(w.R, L)
+    assert s["bound_rows"] == bound == s["cap_rows"]
+    assert s["total_pairs"] == w.NT * w.R
+    rb = W.row_bytes(w)
+    assert s["packed_x_bytes"] == w.N * bound * rb
+    assert s["x_bytes"] == w.NT * rb
+    assert s["pos_bytes"] == w.NT * w.R * 4
+    assert s["send_counts_bytes"] == w.N * w.N * 4
+    if w.x_dtype == W.FP8E4M3_BLK128:
+        assert s["packed_scales_bytes"] == w.N * bound * (w.H // 128) * 4
+    else:
+        assert s["packed_scales_bytes"] == 0
+
+
+def test_explicit_capacity_is_used(lib):
+    s = moe.buffer_sizes(moe.make_dims(4, 64, 16, 2, 1024, cap_rows=100))
+    assert s["cap_rows"] == 100 and s["bound_rows"] == 4 * 64 * 4
+
+
+BAD_DIMS = [
+    (dict(N=3, T=8, E=16, R=2, H=64), moe.MOE_ERR_INVALID_ARG, "multiple of N"),
+    (dict(N=4, T=8, E=16, R=17, H=64), moe.MOE_ERR_INVALID_ARG, "exceeds E"),
+    (dict(N=4, T=8, E=64, R=33, H=64), moe.MOE_ERR_UNSUPPORTED, "R<=32"),
+    (dict(N=4, T=8, E=2048, R=2, H=64), moe.MOE_ERR_UNSUPPORTED, "E<=1024"),
+    (dict(N=4, T=8, E=16, R=2, H=60), moe.MOE_ERR_INVALID_ARG, "multiple of 8"),
+    (dict(N=4, T=8, E=16, R=2, H=64, x_dtype=moe.MOE_FP8E4M3_BLK128), moe.MOE_ERR_INVALID_ARG,
+     "128"),
+    (dict(N=4, T=8, E=16, R=2, H=64, x_dtype=7), moe.MOE_ERR_INVALID_ARG, "x_dtype"),
+    (dict(N=4, T=8, E=16, R=2, H=64, y_dtype=moe.MOE_FP8E4M3_BLK128), moe.MOE_ERR_INVALID_ARG,
+     "y_dtype"),
+    (dict(N=0, T=8, E=16, R=2, H=64), moe.MOE_ERR_INVALID_ARG, "N>=1"),
+    (dict(N=4, T=-1, E=16, R=2, H=64), moe.MOE_ERR_INVALID_ARG, "T>=0"),
+    (dict(N=4, T=8, E=16, R=2, H=64, cap_rows=-5), moe.MOE_ERR_INVALID_ARG, "cap_rows"),
+    (dict(N=64, T=100000, E=384, R=8, H=64), moe.MOE_ERR_UNSUPPORTED, "2^31"),
+]
+
+
+@pytest.mark.parametrize("kw,code,msg", BAD_DIMS)
+def test_bad_dims_are_rejected_on_the_host(lib, kw, code, msg):
+    d = moe.make_dims(**kw)
+    s = moe.MoeSizes()
+    assert lib.moe_buffer_sizes(ctypes.byref(d), ctypes.byref(s)) == code
+    assert msg in lib.moe_last_error().decode()
+    # every compute entry point validates the same way before any CUDA call
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    assert lib.moe_route_topk(ctypes.byref(d), fake, None, 0, 0, fake, fake, None) == code
+    assert lib.moe_dispatch_count(ctypes.byref(d), fake, fake, fake, fake, fake, fake, fake, fake,
+                                  None) == code
+    assert lib.moe_dispatch_pack(ctypes.byref(d), fake, fake, fake, fake, fake, fake, None) == code
+    assert lib.moe_combine(ctypes.byref(d), fake, fake, fake, fake, None) == code
+
+
+def test_reserved_field_must_be_zero(lib):
+    d = moe.make_dims(4, 8, 16, 2, 64)
+    d.reserved = 1
+    s = moe.MoeSizes()
+    assert lib.moe_buffer_sizes(ctypes.byref(d), ctypes.byref(s)) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_null_and_misaligned_pointers_are_rejected(lib):
+    d = moe.make_dims(4, 8, 16, 2, 64)
+    P = ctypes.c_void_p
+    ok, odd, mis16 = P(0x10000), P(0x10002), P(0x10008)
+    E_INV = moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_route_topk(ctypes.byref(d), None, None, 0, 0, ok, ok, None) == E_INV
+    assert lib.moe_route_topk(ctypes.byref(d), odd, None, 0, 0, ok, ok, None) == E_INV
+    assert lib.moe_route_topk(ctypes.byref(d), ok, None, 5, 0, ok, ok, None) == E_INV
+    assert "score_fn" in lib.moe_last_error().decode()
+    assert lib.moe_dispatch_count(ctypes.byref(d), ok, ok, ok, ok, ok, ok, ok, None, None) == E_INV
+    assert lib.moe_dispatch_pack(ctypes.byref(d), mis16, None, ok, ok, None, ok, None) == E_INV
+    assert "16-byte" in lib.moe_last_error().decode()
+    assert lib.moe_dispatch_pack(ctypes.byref(d), ok, None, ok, None, None, ok, None) == E_INV
+    fp8 = moe.make_dims(4, 8, 16, 2, 128, x_dtype=moe.MOE_FP8E4M3_BLK128)
+    assert lib.moe_dispatch_pack(ctypes.byref(fp8), ok, None, ok, ok, None, ok, None) == E_INV
+    assert lib.moe_combine(ctypes.byref(d), ok, ok, ok, mis16, None) == E_INV
+    assert lib.moe_read_status(None, None) == E_INV
+    assert lib.moe_dispatch_pack(None, ok, None, ok, ok, None, ok, None) == E_INV
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    d = moe.make_dims(1, 4, 8, 2, 64)
+    t = torch.zeros(4, 8)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        moe.route_topk(d, t, None, 0, False, t, t)

@@ -1,0 +1,196 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bar: indices, counts, offsets, positions, packed rows and packed_src are
+bit-exact; the status word matches; floats meet these tolerances:
+
+* topk_w: relative 2e-6.  The kernel works in f32: the key difference
+  z - max z is rounded once (error |z - max| * 2^-24, |z - max| <= 4 for
+  selected experts here), expf is within 2 ulp, the softmax denominator is a
+  32-lane butterfly over at most 32 sequential terms per lane (<= 32 + 5
+  roundings on terms that add up to at most E*ulp-scale but weighted by
+  their size -- in practice a few ulp), the division 0.5 ulp, and the
+  renormalisation another sum of <= 32 terms (5 levels) and a division.
+  Summed, about 20 ulp = 1.2e-6 in the worst realistic case; 2e-6 leaves
+  margin while still catching any wrong term.
+* combine, bf16 output: |got - ref| <= 2e-2 + 1e-2 |ref| (ref in fp64).
+* combine, f32 output: |got - ref| <= 1e-5 * sum_k |w_k y_k|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_moe_route_topk_gb300 import workloads as W
+from gpu_path import GpuRun, TOPK_W_RTOL, check_combine, compact_of_region
+from test_oracle_pins import check_count_invariants
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from combine_moe_route_topk_gb300 import _build
+    _build.build()
+    torch.cuda.init()
+
+
+def _oracle_route_count(w, inp):
+    bias = None if inp.bias is None else inp.bias.numpy()
+    idx, tw, _ = oracle.route(inp.logits.numpy(), bias, w.R, w.score_fn, w.renormalize)
+    cnt, st = oracle.count(w.N, w.T, w.E, W.default_cap(w), idx)
+    return idx, tw, cnt, st
+
+
+def _compare(w, inp, topk_idx_override=None, combine_tokens=None):
+    gr = GpuRun(w, inp, topk_idx_override=topk_idx_override)
+    h = gr.host
+    idx, tw, cnt, st = _oracle_route_count(w, inp)
+    # route
+    np.testing.assert_array_equal(h["topk_idx"], idx)
+    np.testing.assert_allclose(h["topk_w"], tw, rtol=TOPK_W_RTOL, atol=0)
+    if topk_idx_override is not None:
+        idx = np.ascontiguousarray(topk_idx_override, np.int32)
+        cnt, st = oracle.count(w.N, w.T, w.E, W.default_cap(w), idx)
+    # count
+    assert gr.status == st
+    for k in ("expert_counts", "expert_offsets", "rank_counts", "rank_offsets", "send_counts",
+              "pos"):
+        np.testing.assert_array_equal(h[k], cnt[k], err_msg=k)
+    cap = gr.cap
+    # pack (only the occupied rows are defined)
+    xb = oracle.x_as_bytes(inp.x)
+    xs = None if inp.x_scales is None else inp.x_scales.numpy()
+    opx, ops, osrc = oracle.pack(xb, xs, cnt["pos"], cnt["rank_offsets"], cap)
+    gpx, gps, gsrc = gr.packed_rows()
+    crow = compact_of_region(gr.rows, cap, cnt["rank_offsets"])
+    np.testing.assert_array_equal(gsrc, osrc[crow])
+    np.testing.assert_array_equal(gpx, opx[crow])
+    if ops is not None:
+        np.testing.assert_array_equal(gps, ops[crow])
+    # combine
+    out = gr.combine()
+    y = oracle.expert_op(w.expert_op, opx, ops, osrc, idx, w.H, w.x_dtype, w.y_dtype)
+    pos, wt = cnt["pos"], tw
+    if combine_tokens is not None:
+        pos, wt = pos[combine_tokens], wt[combine_tokens]
+    ref, mag = oracle.combine(y, w.y_dtype, pos, cnt["rank_offsets"], wt, cap, w.H)
+    check_combine(w, out, ref, mag, combine_tokens)
+    return gr, idx, cnt
+
+
+@pytest.mark.parametrize("name", list(W.WORKLOADS))
+def test_full_size_workload(name):
+    """The five workloads at their full sizes, in the launch configuration the
+    benchmark uses; every output compared."""
+    w = W.WORKLOADS[name]
+    inp = W.make_inputs(w)
+    gr, idx, cnt = _compare(w, inp)
+    assert gr.status == oracle.OK
+    check_count_invariants(w, idx, gr.host, gr.cap)
+
+
+REDUCED = {
+    # ragged everything, f32 rows in and out
+    "ragged_f32": W.Workload("ragged_f32", N=3, T=333, E=48, R=6, H=264, x_dtype=W.F32,
+                             y_dtype=W.F32, renormalize=True, seed=1),
+    # 2 experts per lane (scalar loads), sigmoid + bias, scale expert
+    "scalar_lanes": W.Workload("scalar_lanes", N=5, T=77, E=40, R=3, H=136,
+                               score_fn=W.SIGMOID, bias="normal",
+                               expert_op=W.EXPERT_SCALE, seed=2),
+    # largest E and R the library supports
+    "max_e_r": W.Workload("max_e_r", N=8, T=40, E=1024, R=32, H=64, renormalize=True, seed=3),
+    "r1": W.Workload("r1", N=2, T=100, E=8, R=1, H=128, seed=4),
+    "n1": W.Workload("n1", N=1, T=300, E=64, R=4, H=128, seed=5),
+    # one expert per rank (E/N < R): the bound uses R
+    "e_eq_n": W.Workload("e_eq_n", N=16, T=20, E=16, R=4, H=64, seed=6),
+    "t1": W.Workload("t1", N=7, T=1, E=14, R=2, H=64, seed=7),
+    "fp8_small": W.Workload("fp8_small", N=4, T=50, E=32, R=4, H=384,
+                            x_dtype=W.FP8E4M3_BLK128, expert_op=W.EXPERT_DEQUANT, seed=8),
+    # more tokens than one cluster pass: several tiles per block, ragged
+    "multi_tile": W.Workload("multi_tile", N=4, T=5000, E=64, R=8, H=64, renormalize=True,
+                             seed=9),
+    # R > 8 uses the 512-thread count kernel
+    "r16": W.Workload("r16", N=4, T=600, E=64, R=16, H=64, score_fn=W.SIGMOID, seed=10),
+    # bf16 rows, f32 expert outputs
+    "bf16_to_f32": W.Workload("bf16_to_f32", N=2, T=64, E=16, R=2, H=512, y_dtype=W.F32,
+                              seed=11),
+}
+
+
+@pytest.mark.parametrize("name", list(REDUCED))
+def test_reduced_case(name):
+    w = REDUCED[name]
+    _compare(w, W.make_inputs(w))
+
+
+def test_ties_break_to_lower_index():
+    w = W.WORKLOADS["tiny"].replace(seed=12)
+    inp = W.make_inputs(w, tie_every=3)
+    _compare(w, inp)
+
+
+def test_signed_zero_keys_tie():
+    w = W.Workload("zeros", N=2, T=32, E=32, R=4, H=64, score_fn=W.SIGMOID, seed=13)
+    inp = W.make_inputs(w)
+    inp.logits[:, ::2] = -0.0
+    inp.logits[:, 1::2] = 0.0
+    _compare(w, inp)
+
+
+def test_capacity_overflow_reports_and_drops():
+    w = W.WORKLOADS["tiny"].replace(cap_rows=100, seed=14)
+    inp = W.make_inputs(w)
+    gr, idx, cnt = _compare(w, inp)
+    assert gr.status == oracle.ERR_CAPACITY
+    assert (gr.host["pos"] == -1).any()
+
+
+def test_invalid_expert_ids_are_reported_and_skipped():
+    w = W.Workload("bad", N=4, T=64, E=16, R=3, H=64, seed=15)
+    inp = W.make_inputs(w)
+    bias = None
+    idx, _, _ = oracle.route(inp.logits.numpy(), bias, w.R, w.score_fn, w.renormalize)
+    bad = idx.copy()
+    bad[3, 1] = -1          # below range
+    bad[10, 0] = w.E        # above range
+    bad[20, 2] = bad[20, 0]  # repeated expert inside one token
+    gr, _, cnt = _compare(w, inp, topk_idx_override=bad)
+    assert gr.status == oracle.ERR_INVALID
+    assert gr.host["pos"][3, 1] == -1 and gr.host["pos"][10, 0] == -1
+    assert gr.host["pos"][20, 2] == -1 and gr.host["pos"][20, 0] >= 0
+
+
+def test_empty_batch():
+    import combine_moe_route_topk_gb300 as moe
+    w = W.Workload("empty", N=4, T=0, E=16, R=2, H=64)
+    dims = moe.dims_of(w)
+    b = moe.Buffers(dims)
+    b.expert_counts.fill_(7)
+    b.send_counts.fill_(7)
+    x = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
+    logits = torch.empty(0, 16, dtype=torch.float32, device="cuda")
+    moe.route_topk(dims, logits, None, W.SOFTMAX, False, b.topk_idx, b.topk_w)
+    moe.dispatch_count(dims, b.topk_idx, b.expert_counts, b.expert_offsets, b.rank_counts,
+                       b.rank_offsets, b.send_counts, b.pos, b.status)
+    moe.dispatch_pack(dims, x, None, b.pos, b.packed_x, None, b.packed_src)
+    moe.combine(dims, b.y, b.pos, b.topk_w, b.out)
+    assert moe.read_status(b.status) == moe.MOE_OK
+    assert int(b.expert_counts.abs().sum()) == 0 and int(b.send_counts.abs().sum()) == 0
+    assert b.expert_offsets.cpu().tolist() == [0] * 17
+    assert b.rank_offsets.cpu().tolist() == [0] * 5
+
+
+def test_repeated_calls_are_deterministic():
+    """Same inputs twice -> identical bytes (no scheduling dependence)."""
+    w = W.WORKLOADS["kimi_k2_decode"].replace(H=256)
+    inp = W.make_inputs(w)
+    a = GpuRun(w, inp)
+    b = GpuRun(w, inp)
+    for k in a.host:
+        np.testing.assert_array_equal(a.host[k], b.host[k], err_msg=k)
+    pa, _, sa = a.packed_rows()
+    pb, _, sb = b.packed_rows()
+    np.testing.assert_array_equal(pa, pb)
+    np.testing.assert_array_equal(sa, sb)
+    oa, ob = a.combine().cpu(), b.combine().cpu()
+    assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
