@@ -46,6 +46,9 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="CPU work for the oracle baseline (0 disables it)")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--cap-rows", type=int, default=0,
+                   help="per-rank receive capacity (0: the bound N*T*max(R,E/N)); a smaller "
+                        "capacity shrinks the allocation, not the work")
     return p.parse_args()
 
 
@@ -260,6 +263,8 @@ def run_ours(args):
     moe.lib()  # fails loudly if the library was not built
 
     w = W.WORKLOADS[args.workload]
+    if args.cap_rows:
+        w = w.replace(cap_rows=args.cap_rows)
     dims = moe.dims_of(w)
     inp_cpu = W.make_inputs(w)
     inp = W.Inputs(*(t.to(dev) if t is not None else None
@@ -272,28 +277,52 @@ def run_ours(args):
     def flush():
         flush_buf.fill_(1)
 
+    def launch(k):
+        if k == "route":
+            moe.route_topk(dims, inp.logits, inp.bias, w.score_fn, w.renormalize, b.topk_idx,
+                           b.topk_w, stream)
+        elif k == "count":
+            moe.dispatch_count(dims, b.topk_idx, b.expert_counts, b.expert_offsets,
+                               b.rank_counts, b.rank_offsets, b.send_counts, b.pos, b.status,
+                               stream)
+        elif k == "pack":
+            moe.dispatch_pack(dims, inp.x, inp.x_scales, b.pos, b.packed_x, b.packed_scales,
+                              b.packed_src, stream)
+        else:
+            moe.combine(dims, b.y, b.pos, b.topk_w, b.out, stream)
+
     def step(ev):
+        # dispatch (route -> count -> pack) back to back, so each kernel's
+        # launch overlaps the tail of the previous one; then the expert-op
+        # stand-in (L2 flush, untimed); then combine.
         ev[0].record(stream)
-        moe.route_topk(dims, inp.logits, inp.bias, w.score_fn, w.renormalize, b.topk_idx,
-                       b.topk_w, stream)
+        launch("route")
+        launch("count")
+        launch("pack")
         ev[1].record(stream)
-        moe.dispatch_count(dims, b.topk_idx, b.expert_counts, b.expert_offsets, b.rank_counts,
-                           b.rank_offsets, b.send_counts, b.pos, b.status, stream)
+        flush()
         ev[2].record(stream)
-        moe.dispatch_pack(dims, inp.x, inp.x_scales, b.pos, b.packed_x, b.packed_scales,
-                          b.packed_src, stream)
+        launch("combine")
         ev[3].record(stream)
-        flush()  # expert-op stand-in: nothing survives in L2 between pack and combine
+
+    def step_breakdown(ev):
+        # one event between every two kernels: per-kernel times (the events
+        # serialise the launches, so these sum to a little more than a step)
+        ev[0].record(stream)
+        for i, k in enumerate(("route", "count", "pack")):
+            launch(k)
+            ev[i + 1].record(stream)
+        flush()
         ev[4].record(stream)
-        moe.combine(dims, b.y, b.pos, b.topk_w, b.out, stream)
+        launch("combine")
         ev[5].record(stream)
 
-    def new_events():
-        return [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    def new_events(n=6):
+        return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
 
     for _ in range(max(3, args.warmup)):
         flush()
-        step(new_events())
+        step(new_events(4))
     st = moe.read_status(b.status, stream)
     if st != moe.MOE_OK:
         raise SystemExit(f"dispatch_count status {moe.STATUS_NAMES.get(st, st)} on {w.name}")
@@ -301,7 +330,7 @@ def run_ours(args):
     sampler = None if args.no_clocks else ClockSampler(local_rank)
     if sampler is not None:
         sampler.wait_first()
-    evs = [new_events() for _ in range(args.steps)]
+    evs = [new_events(4) for _ in range(args.steps)]
     if pg:
         pg.barrier()
     torch.cuda.synchronize(dev)
@@ -319,19 +348,31 @@ def run_ours(args):
         sampler.stop()
         clocks = sampler.summary(t_wall0, t_wall1)
 
-    per = {k: [] for k in KERNELS}
-    for ev in evs:
-        per["route"].append(ev[0].elapsed_time(ev[1]))
-        per["count"].append(ev[1].elapsed_time(ev[2]))
-        per["pack"].append(ev[2].elapsed_time(ev[3]))
-        per["combine"].append(ev[4].elapsed_time(ev[5]))
-    step_ms = [sum(per[k][i] for k in KERNELS) for i in range(args.steps)]
+    dispatch_ms = [ev[0].elapsed_time(ev[1]) for ev in evs]
+    combine_ms = [ev[2].elapsed_time(ev[3]) for ev in evs]
+    step_ms = [a + c for a, c in zip(dispatch_ms, combine_ms)]
     ms = statistics.mean(step_ms)
     if pg:
         t = torch.tensor([ms], device=dev, dtype=torch.float64)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         ms = float(t.item())
     value = world * w.NT / (ms / 1e3)
+
+    # per-kernel breakdown, after the timed region
+    nb = max(10, min(args.steps, 200))
+    bevs = [new_events(6) for _ in range(nb)]
+    for i in range(nb):
+        flush()
+        step_breakdown(bevs[i])
+    torch.cuda.synchronize(dev)
+    per = {k: [] for k in KERNELS}
+    for ev in bevs:
+        per["route"].append(ev[0].elapsed_time(ev[1]))
+        per["count"].append(ev[1].elapsed_time(ev[2]))
+        per["pack"].append(ev[2].elapsed_time(ev[3]))
+        per["combine"].append(ev[4].elapsed_time(ev[5]))
+    per_timed = {"dispatch (route+count+pack)": statistics.mean(dispatch_ms),
+                 "combine": statistics.mean(combine_ms)}
 
     # ---- end to end through the public API with host buffers -------------
     e2e = run_e2e(args, w, dims, inp_cpu, b, dev, stream, flush, moe)
@@ -344,12 +385,16 @@ def run_ours(args):
         kern[k] = {"ms": mean_ms, "median_ms": statistics.median(per[k]),
                    "alg_bytes": alg[k], "alg_gbs": alg[k] / (mean_ms / 1e3) / 1e9}
     dom = max(("pack", "combine"), key=lambda k: kern[k]["ms"])
-    achieved = kern[dom]["alg_gbs"]
+    # combine has its own events inside the timed region; pack's come from
+    # the breakdown pass right after it
+    dom_ms = per_timed["combine"] if dom == "combine" else kern["pack"]["ms"]
+    achieved = alg[dom] / (dom_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                 "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
-                "unit": "GB/s", "frac": achieved / peak, "traffic": ncu_traffic(dom, w.name)}
-    pc_ms = kern["pack"]["ms"] + kern["combine"]["ms"]
+                "unit": "GB/s", "frac": achieved / peak, "traffic": ncu_traffic(dom, w.name),
+                "alg_bytes_per_launch": alg[dom], "launch_ms": dom_ms}
+    pc_ms = kern["pack"]["ms"] + per_timed["combine"]
     pc_gbs = (alg["pack"] + alg["combine"]) / (pc_ms / 1e3) / 1e9
 
     if rank != 0:
@@ -369,6 +414,7 @@ def run_ours(args):
         "roofline": roofline,
         "pack_plus_combine": {"ms": pc_ms, "alg_gbs": pc_gbs, "frac": pc_gbs / peak,
                               "frac_of_8tbs_nominal": pc_gbs / 8000.0},
+        "timed_segments_ms": per_timed,
         "kernels": kern,
         "e2e": e2e,
         "cpu_baseline": cpu,

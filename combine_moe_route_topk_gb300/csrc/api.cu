@@ -82,7 +82,7 @@ int check_dims(const MoeDims *d, Derived *out, const char *what) {
     if (v.cap < 1) v.cap = 1;  // T == 0: keep the region arithmetic well defined
     v.pairs = v.NT * d->R;
     v.rows_total = (int64_t)d->N * v.cap;
-    if (v.pairs > kI32Max || v.rows_total > kI32Max)
+    if (v.pairs > kI32Max || v.rows_total > kI32Max || v.NT > kI32Max - 65536)
         return set_error(MOE_ERR_UNSUPPORTED,
                          "%s: N*T*R=%lld and N*cap=%lld must stay below 2^31 (32-bit row indices)",
                          what, (long long)v.pairs, (long long)v.rows_total);

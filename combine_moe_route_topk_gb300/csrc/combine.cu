@@ -13,6 +13,7 @@
 #include <cuda_bf16.h>
 
 #include "moe_internal.cuh"
+#include "pdl.cuh"
 
 namespace moe {
 namespace {
@@ -81,6 +82,8 @@ combine_kernel(const uint4 *__restrict__ y, const int32_t *__restrict__ pos,
     __shared__ int s_pos[32];
     __shared__ float s_w[32];
     const int tid = threadIdx.x;
+    grid_dependency_wait();  // y, pos and topk_w come from earlier kernels
+    grid_launch_dependents();
     for (int64_t g = blockIdx.x; g < NT; g += gridDim.x) {
         if (tid < R) {
             const int p = __ldg(pos + g * R + tid);
@@ -136,15 +139,16 @@ cudaError_t launch_combine(const void *y, int y_dtype, const int32_t *pos, const
     const int elem = (y_dtype == MOE_BF16) ? 2 : 4;
     const int nvec = (int)((int64_t)H * elem / 16);
     const int64_t grid = NT < (int64_t)0x7fffffff ? NT : (int64_t)0x7fffffff;
-    if (y_dtype == MOE_BF16)
-        combine_kernel<1><<<(unsigned)grid, kCombThreads, 0, stream>>>(
-            reinterpret_cast<const uint4 *>(y), pos, topk_w, NT, R, nvec, rows_total,
-            reinterpret_cast<uint4 *>(out));
-    else
-        combine_kernel<0><<<(unsigned)grid, kCombThreads, 0, stream>>>(
-            reinterpret_cast<const uint4 *>(y), pos, topk_w, NT, R, nvec, rows_total,
-            reinterpret_cast<uint4 *>(out));
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kCombThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    auto kern = (y_dtype == MOE_BF16) ? combine_kernel<1> : combine_kernel<0>;
+    return cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const uint4 *>(y), pos, topk_w, NT, R,
+                              nvec, rows_total, reinterpret_cast<uint4 *>(out));
 }
 
 }  // namespace moe

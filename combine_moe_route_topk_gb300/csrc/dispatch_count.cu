@@ -11,45 +11,63 @@
 //
 // One block is not enough parallelism for the larger batches, so the work
 // is split over the C blocks of a cluster (C <= 16) and the blocks exchange
-// their per-expert histograms through distributed shared memory.  The
-// cluster barrier is a hardware barrier, so nothing here spins on memory.
+// their per-expert histograms and per-destination send counts through
+// distributed shared memory.  The cluster barrier is a hardware barrier, so
+// nothing here spins on memory.
 //
 // Ordering (deterministic): rows of rank d are grouped by expert ascending
 // and, inside an expert, by token g ascending.  Token ranges are contiguous
-// per block (block b owns tokens [b*per, (b+1)*per)), so the row of pair
-// (g, k) routed to expert e is
+// per block (block b owns tokens [b*per, (b+1)*per), per a multiple of 32),
+// so the row of pair (g, k) routed to expert e is
 //     d*cap + (expert_offsets[e] - rank_offsets[d])          expert start
 //           + sum over blocks b' < b of hist_b'[e]            earlier blocks
 //           + sum over earlier 32-token groups of this block  earlier groups
 //           + popc(group_mask[e] & lanes below this one)      inside the group
 // where group_mask[e] has bit l set when lane l's token chose e.
+//
+// send_counts[s][d] needs no per-pair atomics when T % 32 == 0: source-rank
+// boundaries then fall on group boundaries, and the pairs rank s sends to
+// rank d are differences of the group prefixes summed over d's experts.
 #include <cooperative_groups.h>
 
 #include "moe_internal.cuh"
+#include "pdl.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace moe {
 namespace {
 
-constexpr int kSendSmem = 4096;  // ints of per-block send matrix staging
+constexpr int kSendSmem = 4096;  // ints of per-block send-count staging
+constexpr int kMaxCluster = 16;
+
+enum SendMode { kSendFromPrefix = 0, kSendSmemAtomics = 1, kSendGlobalAtomics = 2 };
 
 struct CountSmem {
     // byte offsets inside dynamic shared memory
-    int gmask, run, base, tot, eoff, send, flags, bytes;
+    int gmask, subsum, run, base, tot, eoff, fin, send, flags, bytes;
 };
 
-// kWarps 32-token groups per tile (one token per thread).
-__host__ __device__ inline CountSmem count_smem_layout(int E, int kWarps) {
+__host__ __device__ inline int count_ksub(int threads, int E) {
+    const int warps = threads / 32;
+    int k = threads / E;
+    return k >= warps ? warps : (k >= 16 ? 16 : k >= 8 ? 8 : k >= 4 ? 4 : k >= 2 ? 2 : 1);
+}
+
+// kWarps 32-token groups per tile (one token per thread); kSub parts of the
+// group prefix per expert.
+__host__ __device__ inline CountSmem count_smem_layout(int E, int kWarps, int kSub) {
     CountSmem s;
     int o = 0;
-    s.gmask = o; o += kWarps * E * 4;    // u32 [kWarps][E]: group masks, then group prefix
-    s.run = o;   o += E * 4;             // running count of this block per expert
-    s.base = o;  o += E * 4;             // sum over earlier blocks
-    s.tot = o;   o += E * 4;             // sum over all blocks
-    s.eoff = o;  o += (E + 1) * 4 + 12;  // exclusive scan of tot (+ pad to 16 B)
-    s.send = o;  o += kSendSmem * 4;     // staged send_counts rows of this block
-    s.flags = o; o += 64 + 32 * 4;       // [0]: invalid pair seen; [16..48): scan partials
+    s.gmask = o;  o += kWarps * E * 4;     // u32 [kWarps][E]: group masks, then group prefixes
+    s.subsum = o; o += kSub * E * 4;       // group-prefix partial sums
+    s.run = o;    o += 2 * E * 4;          // pairs of this block so far (double buffered)
+    s.base = o;   o += E * 4;              // pairs in earlier blocks
+    s.tot = o;    o += E * 4;              // pairs in all blocks
+    s.eoff = o;   o += (E + 1) * 4 + 12;   // exclusive scan of tot (+ pad to 16 B)
+    s.fin = o;    o += E * 8;              // int2 per expert: first row, rows left before cap
+    s.send = o;   o += kSendSmem * 4;      // this block's send counts, rows s_first..
+    s.flags = o;  o += 64 + 32 * 4;        // [0]: invalid pair seen; [16..48): scan partials
     s.bytes = o;
     return s;
 }
@@ -60,133 +78,226 @@ __device__ __forceinline__ unsigned lanemask_lt() {
     return m;
 }
 
-template <int kCountThreads, int kMaxR>
-__global__ void __launch_bounds__(kCountThreads, 1)
-dispatch_count_kernel(const int32_t *__restrict__ topk_idx, int N, int T, int E, int R,
-                      int64_t cap, int32_t *__restrict__ expert_counts,
-                      int32_t *__restrict__ expert_offsets, int32_t *__restrict__ rank_counts,
-                      int32_t *__restrict__ rank_offsets, int32_t *__restrict__ send_counts,
-                      int32_t *__restrict__ pos, int32_t *__restrict__ status) {
-    constexpr int kWarps = kCountThreads / 32;
+template <int kThreads, int kMaxR>
+__global__ void __launch_bounds__(kThreads, 1)
+dispatch_count_kernel(const int32_t *__restrict__ topk_idx, int N, int T, int E, int R, int cap,
+                      int32_t *__restrict__ expert_counts, int32_t *__restrict__ expert_offsets,
+                      int32_t *__restrict__ rank_counts, int32_t *__restrict__ rank_offsets,
+                      int32_t *__restrict__ send_counts, int32_t *__restrict__ pos,
+                      int32_t *__restrict__ status) {
+    constexpr int kWarps = kThreads / 32;
     extern __shared__ __align__(16) unsigned char smem[];
     cg::cluster_group cluster = cg::this_cluster();
     const int C = (int)cluster.num_blocks();
     const int b = (int)cluster.block_rank();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const CountSmem lay = count_smem_layout(E, kWarps);
+    const int kSub = count_ksub(kThreads, E);
+    const int wps = kWarps / kSub;  // groups per part
+    const CountSmem lay = count_smem_layout(E, kWarps, kSub);
     uint32_t *gmask = reinterpret_cast<uint32_t *>(smem + lay.gmask);
+    int *subsum = reinterpret_cast<int *>(smem + lay.subsum);
     int *run = reinterpret_cast<int *>(smem + lay.run);
     int *sbase = reinterpret_cast<int *>(smem + lay.base);
     int *stot = reinterpret_cast<int *>(smem + lay.tot);
     int *eoff = reinterpret_cast<int *>(smem + lay.eoff);
+    int2 *fin = reinterpret_cast<int2 *>(smem + lay.fin);
     int *ssend = reinterpret_cast<int *>(smem + lay.send);
     int *flags = reinterpret_cast<int *>(smem + lay.flags);
     int *wsum = flags + 16;
 
+    // N*T*R < 2^31 and N*cap < 2^31 are checked on the host: 32-bit math.
     const int L = E / N;
-    const int64_t NT = (int64_t)N * T;
-    const int64_t per = (NT + C - 1) / C;
-    const int64_t lo = min(NT, (int64_t)b * per);
-    const int64_t hi = min(NT, lo + per);
-    const int s_first = (hi > lo) ? (int)(lo / T) : 0;
-    const int span = (hi > lo) ? (int)((hi - 1) / T) - s_first + 1 : 0;
-    const bool send_in_smem = (int64_t)span * N <= kSendSmem;
+    const int NT = N * T;
+    const int per = (((NT + C - 1) / C) + 31) & ~31;  // tokens per block, multiple of 32
+    const int lo = min(NT, b * per);
+    const int hi = min(NT, lo + per);
+    const int s_first = (hi > lo) ? lo / T : 0;
+    const int span = (hi > lo) ? (hi - 1) / T - s_first + 1 : 0;
+    const int max_span = (T > 0) ? (per + T - 1) / T + 1 : 0;  // bound for every block
+    const int mode = (max_span * N > kSendSmem) ? kSendGlobalAtomics
+                     : (T % 32 == 0)            ? kSendFromPrefix
+                                                : kSendSmemAtomics;
+    const bool one_tile = per <= kThreads;
 
-    // ---- phase 0: clear; send_counts is accumulated with atomics below ----
-    for (int i = tid; i < E; i += kCountThreads) run[i] = 0;
-    for (int i = tid; i < kSendSmem; i += kCountThreads) ssend[i] = 0;
+    // ---- phase 0: clear shared state (overlaps the previous kernel's tail)
+    for (int i = tid; i < 2 * E; i += kThreads) run[i] = 0;
+    if (mode != kSendGlobalAtomics)
+        for (int i = tid; i < span * N; i += kThreads) ssend[i] = 0;
     if (tid == 0) flags[0] = 0;
-    for (int64_t i = (int64_t)b * kCountThreads + tid; i < (int64_t)N * N; i += (int64_t)C * kCountThreads)
-        send_counts[i] = 0;
-    cluster.sync();  // zeroed send_counts visible to every block; all blocks running
+    for (int i = tid; i < kWarps * E; i += kThreads) gmask[i] = 0u;
 
-    // ---- phase 1: group masks, in-block ranks, histograms ------------------
+    grid_dependency_wait();  // topk_idx comes from the previous kernel
+    if (mode == kSendGlobalAtomics) {
+        for (int i = b * kThreads + tid; i < N * N; i += C * kThreads) send_counts[i] = 0;
+        cluster.sync();
+    }
+    __syncthreads();
+
+    // ---- phase 1: group masks, in-block ranks, histograms -----------------
     bool bad = false;
-    for (int64_t t0 = lo; t0 < hi; t0 += kCountThreads) {
-        for (int i = tid; i < kWarps * E; i += kCountThreads) gmask[i] = 0u;
-        __syncthreads();
-        const int64_t g = t0 + tid;
+    int ek[kMaxR];    // expert of pair k (-1: invalid), kept for phase 3
+    int part[kMaxR];  // rank of pair k among earlier pairs of this block with that expert
+    int cur = 0;      // run[] buffer holding the counts before this tile
+    for (int t0 = lo; t0 < hi; t0 += kThreads) {
+        const int g = t0 + tid;
         const bool active = g < hi;
-        int ek[kMaxR];
-        int rk[kMaxR];
-        const unsigned bit = 1u << lane;
-        uint32_t *mymask = gmask + warp * E;
+#pragma unroll
+        for (int k = 0; k < kMaxR; ++k) ek[k] = -1;
+        if (active) {
+            const int32_t *row = topk_idx + (int64_t)g * R;
+            if ((R & 3) == 0 && (reinterpret_cast<uintptr_t>(topk_idx) & 15) == 0) {
+#pragma unroll
+                for (int k = 0; k < kMaxR; k += 4) {
+                    if (k < R) {
+                        const int4 v = __ldg(reinterpret_cast<const int4 *>(row + k));
+                        ek[k] = v.x;
+                        ek[k + 1] = v.y;
+                        ek[k + 2] = v.z;
+                        ek[k + 3] = v.w;
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < kMaxR; ++k)
+                    if (k < R) ek[k] = __ldg(row + k);
+            }
+        }
+        if (t0 != lo) {
+            for (int i = tid; i < kWarps * E; i += kThreads) gmask[i] = 0u;
+            __syncthreads();
+        }
+        // validity: in range and not a repeat of an earlier expert of the token
 #pragma unroll
         for (int k = 0; k < kMaxR; ++k) {
-            ek[k] = -1;
-            rk[k] = 0;
             if (k < R && active) {
-                int e = __ldg(topk_idx + g * R + k);
+                const int e = ek[k];
                 bool ok = (e >= 0 && e < E);
-                if (ok) {
-                    unsigned old = atomicOr(mymask + e, bit);
-                    ok = (old & bit) == 0u;  // a repeat of an earlier k of this token
-                }
-                if (ok) {
-                    ek[k] = e;
-                    const int s = (int)(g / T), d = e / L;
-                    if (send_in_smem) atomicAdd(ssend + (s - s_first) * N + d, 1);
-                    else atomicAdd(send_counts + (int64_t)s * N + d, 1);
-                } else {
+#pragma unroll
+                for (int k2 = 0; k2 < k; ++k2) ok = ok && (ek[k2] != e);
+                if (!ok) {
+                    ek[k] = -1;
                     bad = true;
                 }
+            }
+        }
+        const unsigned bit = 1u << lane;
+        uint32_t *mymask = gmask + warp * E;
+        const int s_rel = active ? g / T - s_first : 0;
+#pragma unroll
+        for (int k = 0; k < kMaxR; ++k) {
+            if (k < R && ek[k] >= 0) {
+                atomicOr(mymask + ek[k], bit);
+                if (mode == kSendSmemAtomics) atomicAdd(ssend + s_rel * N + ek[k] / L, 1);
+                else if (mode == kSendGlobalAtomics)
+                    atomicAdd(send_counts + (s_rel + s_first) * N + ek[k] / L, 1);
             }
         }
         __syncwarp();
         const unsigned lt = lanemask_lt();
 #pragma unroll
         for (int k = 0; k < kMaxR; ++k)
-            if (k < R && ek[k] >= 0) rk[k] = __popc(mymask[ek[k]] & lt);
+            part[k] = (k < R && ek[k] >= 0) ? __popc(mymask[ek[k]] & lt) : 0;
         __syncthreads();
-        // per expert: prefix over the 32 groups of this tile, then advance run
-        for (int e = tid; e < E; e += kCountThreads) {
-            int r = run[e];
-#pragma unroll 8
-            for (int w = 0; w < kWarps; ++w) {
+        // group prefix per expert, split into kSub parts of wps groups each:
+        // pass A turns masks into prefixes inside each part and records the
+        // part sums; pass B adds the sums of earlier parts and earlier tiles.
+        for (int i = tid; i < E * kSub; i += kThreads) {
+            const int e = i % E, sub = i / E;
+            int r = 0;
+            for (int w = sub * wps; w < (sub + 1) * wps; ++w) {
                 const uint32_t m = gmask[w * E + e];
                 gmask[w * E + e] = (uint32_t)r;
                 r += __popc(m);
             }
-            run[e] = r;
+            subsum[sub * E + e] = r;
         }
         __syncthreads();
-        if (active) {
+        const int nxt = cur ^ 1;
+        for (int i = tid; i < E * kSub; i += kThreads) {
+            const int e = i % E, sub = i / E;
+            int add = run[cur * E + e];
+            for (int s2 = 0; s2 < sub; ++s2) add += subsum[s2 * E + e];
+            for (int w = sub * wps; w < (sub + 1) * wps; ++w) gmask[w * E + e] += (uint32_t)add;
+            if (sub == kSub - 1) run[nxt * E + e] = add + subsum[sub * E + e];
+        }
+        __syncthreads();
+        if (!one_tile) {
 #pragma unroll
             for (int k = 0; k < kMaxR; ++k)
-                if (k < R) pos[g * R + k] = (ek[k] >= 0) ? (int)mymask[ek[k]] + rk[k] : -1;
+                if (k < R && ek[k] >= 0) part[k] += (int)mymask[ek[k]];
         }
+        if (mode == kSendFromPrefix) {
+            // pairs of source rank s in this tile to expert e: prefix difference
+            // between the groups where s starts and ends; summed into (s, e/L)
+            const int th = min(hi, t0 + kThreads);
+            const int sa = t0 / T, sb = (th - 1) / T;
+            for (int i = tid; i < (sb - sa + 1) * E; i += kThreads) {
+                const int s = sa + i / E, e = i % E;
+                const int w0 = (max(s * T, t0) - t0) >> 5;
+                const int w1 = (min((s + 1) * T, th) - t0) >> 5;
+                const int p1 = (w1 >= kWarps) ? run[nxt * E + e] : (int)gmask[w1 * E + e];
+                const int p0 = (w0 >= kWarps) ? run[nxt * E + e] : (int)gmask[w0 * E + e];
+                if (p1 != p0) atomicAdd(ssend + (s - s_first) * N + e / L, p1 - p0);
+            }
+        }
+        if (!one_tile && active) {
+            // several tiles: park the partial rank in pos until phase 3
+#pragma unroll
+            for (int k = 0; k < kMaxR; ++k)
+                if (k < R) pos[(int64_t)g * R + k] = (ek[k] >= 0) ? part[k] : -1;
+        }
+        cur = nxt;
         __syncthreads();  // gmask is cleared again by the next tile
     }
     if (bad) atomicOr(flags, 1);
-    if (send_in_smem) {
-        for (int i = tid; i < span * N; i += kCountThreads) {
-            const int v = ssend[i];
-            if (v != 0) atomicAdd(send_counts + (int64_t)(s_first + i / N) * N + (i % N), v);
-        }
+    if (cur != 0) {  // leave this block's histogram in run[0..E) for the other blocks
+        for (int e = tid; e < E; e += kThreads) run[e] = run[E + e];
     }
 
-    cluster.sync();  // every block's run[] and flags final
+    cluster.sync();  // every block's histogram, send counts and flags final
 
-    // ---- phase 2: exchange histograms through distributed shared memory ----
-    int any_bad = 0;
-    for (int e = tid; e < E; e += kCountThreads) {
+    // ---- phase 2: exchange through distributed shared memory ----------------
+    for (int e = tid; e < E; e += kThreads) {
+        int v[kMaxCluster];
+#pragma unroll
+        for (int bb = 0; bb < kMaxCluster; ++bb)
+            v[bb] = (bb < C) ? *cluster.map_shared_rank(run + e, bb) : 0;
         int base = 0, tot = 0;
-        for (int bb = 0; bb < C; ++bb) {
-            const int v = *cluster.map_shared_rank(run + e, bb);
-            tot += v;
-            if (bb < b) base += v;
+#pragma unroll
+        for (int bb = 0; bb < kMaxCluster; ++bb) {
+            tot += v[bb];
+            if (bb < b) base += v[bb];
         }
         sbase[e] = base;
         stot[e] = tot;
     }
+    if (mode != kSendGlobalAtomics) {
+        // send_counts[s][d]: add the staged rows of every block whose token
+        // range meets source rank s
+        for (int i = b * kThreads + tid; i < N * N; i += C * kThreads) {
+            const int s = i / N, d = i - (i / N) * N;
+            int sum = 0;
+            if (T > 0) {
+                const int b_lo = (s * T) / per;
+                const int b_hi = min(C - 1, ((s + 1) * T - 1) / per);
+                for (int bb = b_lo; bb <= b_hi; ++bb) {
+                    const int sf = min(NT, bb * per) / T;
+                    sum += *cluster.map_shared_rank(ssend + (s - sf) * N + d, bb);
+                }
+            }
+            send_counts[i] = sum;
+        }
+    }
+    int any_bad = 0;
     if (tid < C) any_bad = *cluster.map_shared_rank(flags, tid);
     any_bad = __syncthreads_or(any_bad);
     cluster.sync();  // no remote shared memory access after this point
+    grid_launch_dependents();
 
     // exclusive scan of stot over experts: thread t sums the kIpt
     // consecutive experts [t*kIpt, t*kIpt + kIpt), then a two-level warp scan
     {
-        constexpr int kIpt = (1024 + kCountThreads - 1) / kCountThreads;  // E <= 1024
+        constexpr int kIpt = (1024 + kThreads - 1) / kThreads;  // E <= 1024
         int v[kIpt];
         int local = 0;
 #pragma unroll
@@ -223,36 +334,82 @@ dispatch_count_kernel(const int32_t *__restrict__ topk_idx, int N, int T, int E,
         }
         __syncthreads();
     }
+    // first row of this block's pairs of expert e, and how many rows the
+    // region of e's rank has left from there
+    int over = 0;
+    for (int e = tid; e < E; e += kThreads) {
+        const int d = e / L;
+        const int local = eoff[e] - eoff[d * L] + sbase[e];
+        fin[e] = make_int2(d * cap + local, cap - local);
+    }
+    for (int d = tid; d < N; d += kThreads)
+        if (eoff[(d + 1) * L] - eoff[d * L] > cap) over = 1;
+    over = __syncthreads_or(over);  // some rank cannot take all its rows
 
     if (b == 0) {
-        int over = 0;
-        for (int e = tid; e < E; e += kCountThreads) {
+        for (int e = tid; e < E; e += kThreads) {
             expert_counts[e] = stot[e];
             expert_offsets[e] = eoff[e];
         }
         if (tid == 0) expert_offsets[E] = eoff[E];
-        for (int d = tid; d < N; d += kCountThreads) {
-            const int rc = eoff[(d + 1) * L] - eoff[d * L];
-            rank_counts[d] = rc;
+        for (int d = tid; d < N; d += kThreads) {
+            rank_counts[d] = eoff[(d + 1) * L] - eoff[d * L];
             rank_offsets[d] = eoff[d * L];
-            if ((int64_t)rc > cap) over = 1;
         }
-        if (tid == 0) rank_offsets[N] = eoff[E];
-        over = __syncthreads_or(over);
-        if (tid == 0) *status = any_bad ? MOE_ERR_INVALID_ARG : (over ? MOE_ERR_CAPACITY : MOE_OK);
+        if (tid == 0) {
+            rank_offsets[N] = eoff[E];
+            *status = any_bad ? MOE_ERR_INVALID_ARG : (over ? MOE_ERR_CAPACITY : MOE_OK);
+        }
     }
 
     // ---- phase 3: final rows --------------------------------------------------
-    for (int64_t t0 = lo; t0 < hi; t0 += kCountThreads) {
-        const int64_t g = t0 + tid;
-        if (g >= hi) continue;
-        for (int k = 0; k < R; ++k) {
-            const int part = pos[g * R + k];  // written by this thread in phase 1
-            if (part < 0) continue;
-            const int e = __ldg(topk_idx + g * R + k);
-            const int d = e / L;
-            const int64_t local = (int64_t)(eoff[e] - eoff[d * L]) + sbase[e] + part;
-            pos[g * R + k] = (local < cap) ? (int)((int64_t)d * cap + local) : -1;
+    if (one_tile) {
+        const int g = lo + tid;
+        const bool active = g < hi;
+        uint32_t *mymask = gmask + warp * E;  // group prefixes of this warp's group
+        if (!over) {
+            // fold each expert's first row into the group prefixes (sequential
+            // shared-memory access), leaving one random read per pair
+            for (int i = tid; i < kWarps * E; i += kThreads) gmask[i] += (uint32_t)fin[i % E].x;
+            __syncthreads();
+        }
+        if (active) {
+            int out[kMaxR];
+#pragma unroll
+            for (int k = 0; k < kMaxR; ++k) {
+                out[k] = -1;
+                if (k < R && ek[k] >= 0) {
+                    if (!over) {
+                        out[k] = (int)mymask[ek[k]] + part[k];
+                    } else {
+                        const int2 f = fin[ek[k]];
+                        const int pr = (int)mymask[ek[k]] + part[k];
+                        out[k] = (pr < f.y) ? f.x + pr : -1;
+                    }
+                }
+            }
+            int32_t *prow = pos + (int64_t)g * R;
+            if ((R & 3) == 0 && (reinterpret_cast<uintptr_t>(pos) & 15) == 0) {
+#pragma unroll
+                for (int k = 0; k < kMaxR; k += 4)
+                    if (k < R)
+                        *reinterpret_cast<int4 *>(prow + k) = make_int4(out[k], out[k + 1], out[k + 2], out[k + 3]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < kMaxR; ++k)
+                    if (k < R) prow[k] = out[k];
+            }
+        }
+    } else {
+        for (int t0 = lo; t0 < hi; t0 += kThreads) {
+            const int g = t0 + tid;
+            if (g >= hi) continue;
+            for (int k = 0; k < R; ++k) {
+                const int pr = pos[(int64_t)g * R + k];  // parked by this thread in phase 1
+                if (pr < 0) continue;
+                const int2 f = fin[__ldg(topk_idx + (int64_t)g * R + k)];
+                pos[(int64_t)g * R + k] = (pr < f.y) ? f.x + pr : -1;
+            }
         }
     }
 }
@@ -301,11 +458,11 @@ int max_cluster_blocks(size_t smem_bytes) {
 }
 
 template <int kThreads, int kMaxR>
-cudaError_t launch_count(const int32_t *topk_idx, int N, int T, int E, int R, int64_t cap,
+cudaError_t launch_count(const int32_t *topk_idx, int N, int T, int E, int R, int cap,
                          int32_t *expert_counts, int32_t *expert_offsets, int32_t *rank_counts,
                          int32_t *rank_offsets, int32_t *send_counts, int32_t *pos,
                          int32_t *status, cudaStream_t stream) {
-    const CountSmem lay = count_smem_layout(E, kThreads / 32);
+    const CountSmem lay = count_smem_layout(E, kThreads / 32, count_ksub(kThreads, E));
     const size_t smem = (size_t)lay.bytes;
     const int cmax = max_cluster_blocks<kThreads, kMaxR>(smem);
     if (cmax <= 0) return cudaErrorNotSupported;
@@ -319,13 +476,14 @@ cudaError_t launch_count(const int32_t *topk_idx, int N, int T, int E, int R, in
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = c;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1] = pdl_attribute();
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, dispatch_count_kernel<kThreads, kMaxR>, topk_idx, N, T, E, R,
                               cap, expert_counts, expert_offsets, rank_counts, rank_offsets,
                               send_counts, pos, status);
@@ -338,12 +496,24 @@ cudaError_t launch_dispatch_count(const int32_t *topk_idx, int N, int T, int E, 
                                   int32_t *rank_counts, int32_t *rank_offsets,
                                   int32_t *send_counts, int32_t *pos, int32_t *status,
                                   cudaStream_t stream) {
-    // R <= 8 keeps the per-pair state of a thread in registers at 1024
-    // threads per block; larger R uses 512-thread blocks.
-    if (R <= 8)
-        return launch_count<1024, 8>(topk_idx, N, T, E, R, cap, expert_counts, expert_offsets,
+    // cap < 2^31 / N is checked by the caller
+    const int icap = (int)cap;
+    const int64_t NT = (int64_t)N * T;
+    // R <= 8 keeps the per-pair state of a thread in registers.  Batches that
+    // fit one token per thread in a 16-block cluster of 256-thread blocks use
+    // that shape (less serial work per SM); larger ones use 1024-thread
+    // blocks; R > 8 uses 512-thread blocks.
+    if (R <= 8) {
+        if (NT <= 16 * 256) {
+            const CountSmem lay = count_smem_layout(E, 256 / 32, count_ksub(256, E));
+            if (max_cluster_blocks<256, 8>((size_t)lay.bytes) * 256 >= NT)
+                return launch_count<256, 8>(topk_idx, N, T, E, R, icap, expert_counts, expert_offsets,
+                                            rank_counts, rank_offsets, send_counts, pos, status, stream);
+        }
+        return launch_count<1024, 8>(topk_idx, N, T, E, R, icap, expert_counts, expert_offsets,
                                      rank_counts, rank_offsets, send_counts, pos, status, stream);
-    return launch_count<512, 32>(topk_idx, N, T, E, R, cap, expert_counts, expert_offsets,
+    }
+    return launch_count<512, 32>(topk_idx, N, T, E, R, icap, expert_counts, expert_offsets,
                                  rank_counts, rank_offsets, send_counts, pos, status, stream);
 }
 

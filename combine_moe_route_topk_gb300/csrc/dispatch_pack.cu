@@ -13,6 +13,7 @@
 // vectors (every row starts on a 16-byte boundary because H*elem % 16 == 0),
 // keeping all of their loads of a row in flight before issuing the R stores.
 #include "moe_internal.cuh"
+#include "pdl.cuh"
 
 namespace moe {
 namespace {
@@ -35,6 +36,8 @@ dispatch_pack_kernel(const uint4 *__restrict__ x, const float *__restrict__ x_sc
                      float *__restrict__ packed_scales, int32_t *__restrict__ packed_src) {
     __shared__ int s_pos[32];
     const int tid = threadIdx.x;
+    grid_dependency_wait();  // pos comes from the count kernel
+    grid_launch_dependents();
     for (int64_t g = blockIdx.x; g < NT; g += gridDim.x) {
         if (tid < R) {
             const int p = __ldg(pos + g * R + tid);
@@ -82,10 +85,16 @@ cudaError_t launch_dispatch_pack(const void *x, const float *x_scales, const int
     if (NT == 0) return cudaSuccess;
     const int nvec = (int)(row_bytes / 16);
     const int64_t grid = NT < (int64_t)0x7fffffff ? NT : (int64_t)0x7fffffff;
-    dispatch_pack_kernel<<<(unsigned)grid, kPackThreads, 0, stream>>>(
-        reinterpret_cast<const uint4 *>(x), x_scales, pos, NT, R, nvec, scales_per_row, rows_total,
-        reinterpret_cast<uint4 *>(packed_x), packed_scales, packed_src);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kPackThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, dispatch_pack_kernel, reinterpret_cast<const uint4 *>(x),
+                              x_scales, pos, NT, R, nvec, scales_per_row, rows_total,
+                              reinterpret_cast<uint4 *>(packed_x), packed_scales, packed_src);
 }
 
 }  // namespace moe

@@ -12,9 +12,15 @@
 // compile-time constant with 32*J >= E.  Because lower lanes own lower
 // expert ids, "highest key, then lowest lane, then lowest slot" is exactly
 // "highest z, then lowest expert index" -- the tie rule of the definition.
+//
+// Keys: z = fl32(logit + bias) is mapped to an unsigned integer whose order
+// is the float order (-0 is first turned into +0 so that the two zeros tie,
+// as they compare equal).  One round is then a single warp max reduction
+// (redux.sync) plus a ballot for the lowest lane holding the maximum.
 #include <math.h>
 
 #include "moe_internal.cuh"
+#include "pdl.cuh"
 
 namespace moe {
 namespace {
@@ -22,15 +28,27 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kRouteThreads = 256;  // 8 tokens per block
 
+__device__ __forceinline__ uint32_t order_key(float v) {
+    const uint32_t u = __float_as_uint(__fadd_rn(v, 0.0f));  // -0 -> +0
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Highest live key of this lane and its slot (lowest slot among equals);
+// jb = -1 when no slot is live.
 template <int J>
-__device__ __forceinline__ void local_best(const float (&z)[J], uint32_t live, float &v, int &jb) {
-    v = -INFINITY;
+__device__ __forceinline__ void local_best(const uint32_t (&key)[J], uint32_t live, uint32_t &v,
+                                           int &jb) {
+    v = 0u;
     jb = -1;
 #pragma unroll
     for (int j = 0; j < J; ++j) {
         if ((live >> j) & 1u) {
-            if (jb < 0 || z[j] > v) {  // strict '>' keeps the lowest slot on ties
-                v = z[j];
+            if (jb < 0 || key[j] > v) {
+                v = key[j];
                 jb = j;
             }
         }
@@ -42,6 +60,8 @@ __global__ void __launch_bounds__(kRouteThreads)
 route_topk_kernel(const float *__restrict__ logits, const float *__restrict__ bias, int64_t NT,
                   int E, int R, int score_fn, int renormalize, int32_t *__restrict__ topk_idx,
                   float *__restrict__ topk_w) {
+    grid_dependency_wait();  // logits / outputs are shared with earlier kernels
+    grid_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t g = (int64_t)blockIdx.x * (kRouteThreads / 32) + (threadIdx.x >> 5);
     if (g >= NT) return;  // uniform per warp
@@ -49,16 +69,15 @@ route_topk_kernel(const float *__restrict__ logits, const float *__restrict__ bi
     const float *row = logits + g * E;
     const int e0 = lane * J;
     float z[J];
-    uint32_t valid = 0;
 #pragma unroll
-    for (int j = 0; j < J; ++j) z[j] = -INFINITY;
+    for (int j = 0; j < J; ++j) z[j] = 0.f;
     if (kVec4) {
         // E % 4 == 0 and J % 4 == 0: e0 + j is a multiple of 4, so the
         // 16-byte load is aligned and stays inside the row.
 #pragma unroll
         for (int j = 0; j < J; j += 4) {
             if (e0 + j < E) {
-                float4 v = __ldg(reinterpret_cast<const float4 *>(row + e0 + j));
+                const float4 v = __ldg(reinterpret_cast<const float4 *>(row + e0 + j));
                 z[j] = v.x;
                 z[j + 1] = v.y;
                 z[j + 2] = v.z;
@@ -70,32 +89,32 @@ route_topk_kernel(const float *__restrict__ logits, const float *__restrict__ bi
         for (int j = 0; j < J; ++j)
             if (e0 + j < E) z[j] = __ldg(row + e0 + j);
     }
+    uint32_t valid = 0;
+    uint32_t key[J];
 #pragma unroll
     for (int j = 0; j < J; ++j) {
+        key[j] = 0u;
         if (e0 + j < E) {
             valid |= 1u << j;
             if (bias != nullptr) z[j] = __fadd_rn(z[j], __ldg(bias + e0 + j));
+            key[j] = order_key(z[j]);
         }
     }
 
-    // R rounds of warp arg-max.  Each lane keeps its own best live slot and
-    // only the winning lane rescans after a round.
+    // R rounds of warp arg-max; only the winning lane rescans its slots.
     uint32_t live = valid;
-    float v;
+    uint32_t v;
     int jb;
-    local_best<J>(z, live, v, jb);
+    local_best<J>(key, live, v, jb);
     float zmax = 0.f;
     int my_e = 0;
     float my_z = 0.f;
     for (int k = 0; k < R; ++k) {
-        float vmax = v;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, off));
-        unsigned ball = __ballot_sync(kFull, jb >= 0 && v == vmax);
-        if (ball == 0u) ball = __ballot_sync(kFull, jb >= 0);  // only with NaN keys
-        const int wl = __ffs(ball) - 1;
+        const uint32_t kmax = __reduce_max_sync(kFull, v);
+        const unsigned ball = __ballot_sync(kFull, jb >= 0 && v == kmax);
+        const int wl = __ffs(ball) - 1;  // some lane always has a live slot (R <= E)
         const int wj = __shfl_sync(kFull, jb, wl);
-        const float wz = __shfl_sync(kFull, v, wl);
+        const float wz = key_value(kmax);
         if (k == 0) zmax = wz;
         if (lane == k) {
             my_e = wl * J + wj;
@@ -103,7 +122,7 @@ route_topk_kernel(const float *__restrict__ logits, const float *__restrict__ bi
         }
         if (lane == wl) {
             live &= ~(1u << wj);
-            local_best<J>(z, live, v, jb);
+            local_best<J>(key, live, v, jb);
         }
     }
 
@@ -112,7 +131,7 @@ route_topk_kernel(const float *__restrict__ logits, const float *__restrict__ bi
         float s = 0.f;
 #pragma unroll
         for (int j = 0; j < J; ++j)
-            if ((valid >> j) & 1u) s += expf(z[j] - zmax);
+            if ((valid >> j) & 1u) s += expf(key_value(key[j]) - zmax);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
         if (lane < R) p = expf(my_z - zmax) / s;
@@ -131,20 +150,32 @@ route_topk_kernel(const float *__restrict__ logits, const float *__restrict__ bi
     }
 }
 
+template <int J, bool kVec4>
+cudaError_t launch_jv(const float *logits, const float *bias, int64_t NT, int E, int R,
+                      int score_fn, int renormalize, int32_t *topk_idx, float *topk_w,
+                      cudaStream_t stream) {
+    const int64_t blocks = (NT + kRouteThreads / 32 - 1) / (kRouteThreads / 32);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kRouteThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, route_topk_kernel<J, kVec4>, logits, bias, NT, E, R, score_fn,
+                              renormalize, topk_idx, topk_w);
+}
+
 template <int J>
 cudaError_t launch_j(const float *logits, const float *bias, int64_t NT, int E, int R, int score_fn,
                      int renormalize, int32_t *topk_idx, float *topk_w, cudaStream_t stream) {
-    const int64_t blocks = (NT + kRouteThreads / 32 - 1) / (kRouteThreads / 32);
-    const bool vec4 = (J % 4 == 0) && (E % 4 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15) == 0);
-    if (vec4) {
-        if constexpr (J % 4 == 0)
-            route_topk_kernel<J, true><<<(unsigned)blocks, kRouteThreads, 0, stream>>>(
-                logits, bias, NT, E, R, score_fn, renormalize, topk_idx, topk_w);
-    } else {
-        route_topk_kernel<J, false><<<(unsigned)blocks, kRouteThreads, 0, stream>>>(
-            logits, bias, NT, E, R, score_fn, renormalize, topk_idx, topk_w);
+    if constexpr (J % 4 == 0) {
+        if (E % 4 == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0)
+            return launch_jv<J, true>(logits, bias, NT, E, R, score_fn, renormalize, topk_idx,
+                                      topk_w, stream);
     }
-    return cudaGetLastError();
+    return launch_jv<J, false>(logits, bias, NT, E, R, score_fn, renormalize, topk_idx, topk_w,
+                               stream);
 }
 
 }  // namespace

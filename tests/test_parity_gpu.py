@@ -45,11 +45,13 @@ def _compare(w, inp, topk_idx_override=None, combine_tokens=None):
     gr = GpuRun(w, inp, topk_idx_override=topk_idx_override)
     h = gr.host
     idx, tw, cnt, st = _oracle_route_count(w, inp)
-    # route
-    np.testing.assert_array_equal(h["topk_idx"], idx)
+    # route (the count input is replaced afterwards when a test overrides it)
     np.testing.assert_allclose(h["topk_w"], tw, rtol=TOPK_W_RTOL, atol=0)
-    if topk_idx_override is not None:
+    if topk_idx_override is None:
+        np.testing.assert_array_equal(h["topk_idx"], idx)
+    else:
         idx = np.ascontiguousarray(topk_idx_override, np.int32)
+        np.testing.assert_array_equal(h["topk_idx"], idx)
         cnt, st = oracle.count(w.N, w.T, w.E, W.default_cap(w), idx)
     # count
     assert gr.status == st
