@@ -61,6 +61,23 @@ def dist_info():
             int(os.environ.get("WORLD_SIZE", 1)))
 
 
+def reduce_max(value: float, dist=None) -> float:
+    """Max of `value` over all ranks (the slowest replica sets the step
+    time).  Works with NCCL (CUDA tensor) and gloo (CPU tensor)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_replica: int, world: int, ms_per_step: float) -> float:
+    """Whole-job tokens/s: every replica processes its own batch per step."""
+    return world * tokens_per_replica / (ms_per_step / 1e3)
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -357,12 +374,8 @@ def run_ours(args):
     dispatch_ms = [ev[0].elapsed_time(ev[1]) for ev in evs]
     combine_ms = [ev[2].elapsed_time(ev[3]) for ev in evs]
     step_ms = [a + c for a, c in zip(dispatch_ms, combine_ms)]
-    ms = statistics.mean(step_ms)
-    if pg:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * w.NT / (ms / 1e3)
+    ms = reduce_max(statistics.mean(step_ms), pg)
+    value = job_throughput(w.NT, world, ms)
 
     # per-kernel breakdown, after the timed region
     nb = max(10, min(args.steps, 200))

@@ -104,6 +104,7 @@ dispatch_count_kernel(const int32_t *__restrict__ topk_idx, int N, int T, int E,
     int *ssend = reinterpret_cast<int *>(smem + lay.send);
     int *flags = reinterpret_cast<int *>(smem + lay.flags);
     int *wsum = flags + 16;
+    __shared__ int sfirst_tab[kMaxCluster];  // first source rank of each block
 
     // N*T*R < 2^31 and N*cap < 2^31 are checked on the host: 32-bit math.
     const int L = E / N;
@@ -120,6 +121,7 @@ dispatch_count_kernel(const int32_t *__restrict__ topk_idx, int N, int T, int E,
     const bool one_tile = per <= kThreads;
 
     // ---- phase 0: clear shared state (overlaps the previous kernel's tail)
+    if (tid < kMaxCluster) sfirst_tab[tid] = (T > 0) ? min(NT, tid * per) / T : 0;
     for (int i = tid; i < 2 * E; i += kThreads) run[i] = 0;
     if (mode != kSendGlobalAtomics)
         for (int i = tid; i < span * N; i += kThreads) ssend[i] = 0;
@@ -198,47 +200,69 @@ dispatch_count_kernel(const int32_t *__restrict__ topk_idx, int N, int T, int E,
         for (int k = 0; k < kMaxR; ++k)
             part[k] = (k < R && ek[k] >= 0) ? __popc(mymask[ek[k]] & lt) : 0;
         __syncthreads();
-        // group prefix per expert, split into kSub parts of wps groups each:
-        // pass A turns masks into prefixes inside each part and records the
-        // part sums; pass B adds the sums of earlier parts and earlier tiles.
-        for (int i = tid; i < E * kSub; i += kThreads) {
-            const int e = i % E, sub = i / E;
-            int r = 0;
-            for (int w = sub * wps; w < (sub + 1) * wps; ++w) {
-                const uint32_t m = gmask[w * E + e];
-                gmask[w * E + e] = (uint32_t)r;
-                r += __popc(m);
-            }
-            subsum[sub * E + e] = r;
-        }
-        __syncthreads();
+        // group prefix per expert, split into kSub parts of wps groups each.
+        // Pass A turns the masks of a part into prefixes inside the part (all
+        // loads first) and, when source ranks start on group boundaries,
+        // adds each group's pairs to the send count of the group's rank.
+        // With kSub > 1, pass B adds the sums of earlier parts.
         const int nxt = cur ^ 1;
         for (int i = tid; i < E * kSub; i += kThreads) {
-            const int e = i % E, sub = i / E;
-            int add = run[cur * E + e];
-            for (int s2 = 0; s2 < sub; ++s2) add += subsum[s2 * E + e];
-            for (int w = sub * wps; w < (sub + 1) * wps; ++w) gmask[w * E + e] += (uint32_t)add;
-            if (sub == kSub - 1) run[nxt * E + e] = add + subsum[sub * E + e];
+            const int sub = i / E, e = i - sub * E;
+            const int wb = sub * wps;
+            int r = (kSub == 1) ? run[cur * E + e] : 0;
+            // send-count walk state: source rank of the current group, tokens
+            // of that rank seen so far in this part, pairs not yet flushed
+            const int g0 = t0 + 32 * wb;
+            int s_cur = g0 / T, rem = g0 - s_cur * T, acc = 0;
+            const int d = e / L;
+            auto flush = [&]() {  // pending pairs of (s_cur, d)
+                if (acc) atomicAdd(ssend + (s_cur - s_first) * N + d, acc);
+                acc = 0;
+            };
+            for (int j0 = 0; j0 < wps; j0 += 8) {  // 8 groups at a time: loads first
+                int c[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    c[j] = (j0 + j < wps) ? __popc(gmask[(wb + j0 + j) * E + e]) : 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (j0 + j < wps) {
+                        gmask[(wb + j0 + j) * E + e] = (uint32_t)r;
+                        r += c[j];
+                        if (mode == kSendFromPrefix && g0 + 32 * (j0 + j) < hi) {
+                            if (rem == T) {  // this group starts the next source rank
+                                flush();
+                                ++s_cur;
+                                rem = 0;
+                            }
+                            acc += c[j];
+                            rem += 32;
+                        }
+                    }
+                }
+            }
+            if (mode == kSendFromPrefix) flush();
+            if (kSub == 1) run[nxt * E + e] = r;
+            else subsum[sub * E + e] = r;
+        }
+        if (kSub > 1) {
+            __syncthreads();
+            for (int i = tid; i < E * kSub; i += kThreads) {
+                const int sub = i / E, e = i - sub * E;
+                const int wb = sub * wps;
+                int add = run[cur * E + e];
+                for (int s2 = 0; s2 < sub; ++s2) add += subsum[s2 * E + e];
+#pragma unroll
+                for (int j = 0; j < kWarps; ++j)
+                    if (j < wps) gmask[(wb + j) * E + e] += (uint32_t)add;
+                if (sub == kSub - 1) run[nxt * E + e] = add + subsum[sub * E + e];
+            }
         }
         __syncthreads();
         if (!one_tile) {
 #pragma unroll
             for (int k = 0; k < kMaxR; ++k)
                 if (k < R && ek[k] >= 0) part[k] += (int)mymask[ek[k]];
-        }
-        if (mode == kSendFromPrefix) {
-            // pairs of source rank s in this tile to expert e: prefix difference
-            // between the groups where s starts and ends; summed into (s, e/L)
-            const int th = min(hi, t0 + kThreads);
-            const int sa = t0 / T, sb = (th - 1) / T;
-            for (int i = tid; i < (sb - sa + 1) * E; i += kThreads) {
-                const int s = sa + i / E, e = i % E;
-                const int w0 = (max(s * T, t0) - t0) >> 5;
-                const int w1 = (min((s + 1) * T, th) - t0) >> 5;
-                const int p1 = (w1 >= kWarps) ? run[nxt * E + e] : (int)gmask[w1 * E + e];
-                const int p0 = (w0 >= kWarps) ? run[nxt * E + e] : (int)gmask[w0 * E + e];
-                if (p1 != p0) atomicAdd(ssend + (s - s_first) * N + e / L, p1 - p0);
-            }
         }
         if (!one_tile && active) {
             // several tiles: park the partial rank in pos until phase 3
@@ -257,53 +281,108 @@ dispatch_count_kernel(const int32_t *__restrict__ topk_idx, int N, int T, int E,
     cluster.sync();  // every block's histogram, send counts and flags final
 
     // ---- phase 2: exchange through distributed shared memory ----------------
-    for (int e = tid; e < E; e += kThreads) {
-        int v[kMaxCluster];
-#pragma unroll
-        for (int bb = 0; bb < kMaxCluster; ++bb)
-            v[bb] = (bb < C) ? *cluster.map_shared_rank(run + e, bb) : 0;
-        int base = 0, tot = 0;
-#pragma unroll
-        for (int bb = 0; bb < kMaxCluster; ++bb) {
-            tot += v[bb];
-            if (bb < b) base += v[bb];
-        }
-        sbase[e] = base;
-        stot[e] = tot;
-    }
-    if (mode != kSendGlobalAtomics) {
-        // send_counts[s][d]: add the staged rows of every block whose token
-        // range meets source rank s
-        for (int i = b * kThreads + tid; i < N * N; i += C * kThreads) {
-            const int s = i / N, d = i - (i / N) * N;
-            int sum = 0;
-            if (T > 0) {
-                const int b_lo = (s * T) / per;
-                const int b_hi = min(C - 1, ((s + 1) * T - 1) / per);
-                for (int bb = b_lo; bb <= b_hi; ++bb) {
-                    const int sf = min(NT, bb * per) / T;
-                    sum += *cluster.map_shared_rank(ssend + (s - sf) * N + d, bb);
-                }
+    // Every remote load of one item is issued before any of them is used.
+    // Small blocks handle an expert and a send_counts entry per iteration so
+    // that both sets of remote loads overlap; 1024-thread blocks (64
+    // registers per thread) handle them in two loops.
+    if constexpr (kThreads <= 256) {
+        const bool smem_send = mode != kSendGlobalAtomics;
+        const int n_e = (E + kThreads - 1) / kThreads;
+        const int n_p = smem_send ? (N * N + C * kThreads - 1) / (C * kThreads) : 0;
+        const int iters = max(n_e, n_p);
+        for (int it = 0; it < iters; ++it) {
+            const int e = tid + it * kThreads;
+            const int i = b * kThreads + tid + it * C * kThreads;
+            const bool do_e = e < E;
+            const bool do_p = smem_send && i < N * N;
+            int s = 0, d = 0, b_lo = 0, b_hi = -1;
+            if (do_p && T > 0) {  // T == 0: no tokens, the count is 0
+                s = i / N;
+                d = i - s * N;
+                b_lo = (s * T) / per;
+                b_hi = min(C - 1, ((s + 1) * T - 1) / per);
             }
-            send_counts[i] = sum;
+            int ve[kMaxCluster], vp[kMaxCluster];
+#pragma unroll
+            for (int bb = 0; bb < kMaxCluster; ++bb) {
+                ve[bb] = (do_e && bb < C) ? *cluster.map_shared_rank(run + e, bb) : 0;
+                const int blk = b_lo + bb;
+                vp[bb] = (blk <= b_hi) ? *cluster.map_shared_rank(ssend + (s - sfirst_tab[blk]) * N + d, blk) : 0;
+            }
+            if (do_e) {
+                int base = 0, tot = 0;
+#pragma unroll
+                for (int bb = 0; bb < kMaxCluster; ++bb) {
+                    tot += ve[bb];
+                    if (bb < b) base += ve[bb];
+                }
+                sbase[e] = base;
+                stot[e] = tot;
+            }
+            if (do_p) {
+                int sum = 0;
+#pragma unroll
+                for (int bb = 0; bb < kMaxCluster; ++bb) sum += vp[bb];
+                send_counts[i] = sum;
+            }
+        }
+    } else {
+        for (int e = tid; e < E; e += kThreads) {
+            int v[kMaxCluster];
+#pragma unroll
+            for (int bb = 0; bb < kMaxCluster; ++bb)
+                v[bb] = (bb < C) ? *cluster.map_shared_rank(run + e, bb) : 0;
+            int base = 0, tot = 0;
+#pragma unroll
+            for (int bb = 0; bb < kMaxCluster; ++bb) {
+                tot += v[bb];
+                if (bb < b) base += v[bb];
+            }
+            sbase[e] = base;
+            stot[e] = tot;
+        }
+        if (mode != kSendGlobalAtomics) {
+            // send_counts[s][d]: add the staged counts of every block whose
+            // token range meets source rank s
+            for (int i = b * kThreads + tid; i < N * N; i += C * kThreads) {
+                const int s = i / N, d = i - (i / N) * N;
+                int b_lo = 0, b_hi = -1;  // T == 0: no tokens, the count is 0
+                if (T > 0) {
+                    b_lo = (s * T) / per;
+                    b_hi = min(C - 1, ((s + 1) * T - 1) / per);
+                }
+                int v[kMaxCluster];
+#pragma unroll
+                for (int bb = 0; bb < kMaxCluster; ++bb) {
+                    const int blk = b_lo + bb;
+                    v[bb] = (blk <= b_hi) ? *cluster.map_shared_rank(ssend + (s - sfirst_tab[blk]) * N + d, blk) : 0;
+                }
+                int sum = 0;
+#pragma unroll
+                for (int bb = 0; bb < kMaxCluster; ++bb) sum += v[bb];
+                send_counts[i] = sum;
+            }
         }
     }
     int any_bad = 0;
     if (tid < C) any_bad = *cluster.map_shared_rank(flags, tid);
     any_bad = __syncthreads_or(any_bad);
-    cluster.sync();  // no remote shared memory access after this point
+    // this block reads no remote shared memory after this point; it waits for
+    // the others to say the same only before exiting
+    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
     grid_launch_dependents();
 
-    // exclusive scan of stot over experts: thread t sums the kIpt
-    // consecutive experts [t*kIpt, t*kIpt + kIpt), then a two-level warp scan
+    // exclusive scan of stot over experts: thread t sums the ipt consecutive
+    // experts [t*ipt, t*ipt + ipt), then a two-level warp scan
     {
-        constexpr int kIpt = (1024 + kThreads - 1) / kThreads;  // E <= 1024
-        int v[kIpt];
+        constexpr int kIptMax = (1024 + kThreads - 1) / kThreads;  // E <= 1024
+        const int ipt = (E + kThreads - 1) / kThreads;
+        int v[kIptMax];
         int local = 0;
 #pragma unroll
-        for (int i = 0; i < kIpt; ++i) {
-            const int e = tid * kIpt + i;
-            v[i] = (e < E) ? stot[e] : 0;
+        for (int i = 0; i < kIptMax; ++i) {
+            const int e = tid * ipt + i;
+            v[i] = (i < ipt && e < E) ? stot[e] : 0;
             local += v[i];
         }
         int x = local;
@@ -326,25 +405,35 @@ dispatch_count_kernel(const int32_t *__restrict__ topk_idx, int N, int T, int E,
         __syncthreads();
         int run_e = x - local + (warp > 0 ? wsum[warp - 1] : 0);  // exclusive start
 #pragma unroll
-        for (int i = 0; i < kIpt; ++i) {
-            const int e = tid * kIpt + i;
-            if (e < E) eoff[e] = run_e;
-            run_e += v[i];
-            if (e == E - 1) eoff[E] = run_e;
+        for (int i = 0; i < kIptMax; ++i) {
+            const int e = tid * ipt + i;
+            if (i < ipt && e < E) {
+                eoff[e] = run_e;
+                run_e += v[i];
+                if (e == E - 1) eoff[E] = run_e;
+            }
         }
         __syncthreads();
     }
-    // first row of this block's pairs of expert e, and how many rows the
-    // region of e's rank has left from there
+
+    // does some rank receive more rows than its region holds?
     int over = 0;
+    for (int d = tid; d < N; d += kThreads)
+        if (eoff[(d + 1) * L] - eoff[d * L] > cap) over = 1;
+    over = __syncthreads_or(over);
+    // first row of this block's pairs of expert e and the rows its rank's
+    // region has left from there; without overflow the first row is folded
+    // into the group prefixes so that phase 3 reads one word per pair
     for (int e = tid; e < E; e += kThreads) {
         const int d = e / L;
         const int local = eoff[e] - eoff[d * L] + sbase[e];
         fin[e] = make_int2(d * cap + local, cap - local);
+        if (!over && one_tile) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) gmask[w * E + e] += (uint32_t)(d * cap + local);
+        }
     }
-    for (int d = tid; d < N; d += kThreads)
-        if (eoff[(d + 1) * L] - eoff[d * L] > cap) over = 1;
-    over = __syncthreads_or(over);  // some rank cannot take all its rows
+    __syncthreads();
 
     if (b == 0) {
         for (int e = tid; e < E; e += kThreads) {
@@ -367,12 +456,6 @@ dispatch_count_kernel(const int32_t *__restrict__ topk_idx, int N, int T, int E,
         const int g = lo + tid;
         const bool active = g < hi;
         uint32_t *mymask = gmask + warp * E;  // group prefixes of this warp's group
-        if (!over) {
-            // fold each expert's first row into the group prefixes (sequential
-            // shared-memory access), leaving one random read per pair
-            for (int i = tid; i < kWarps * E; i += kThreads) gmask[i] += (uint32_t)fin[i % E].x;
-            __syncthreads();
-        }
         if (active) {
             int out[kMaxR];
 #pragma unroll
@@ -412,6 +495,9 @@ dispatch_count_kernel(const int32_t *__restrict__ topk_idx, int N, int T, int E,
             }
         }
     }
+    // keep this block's shared memory alive until every block has finished
+    // reading it
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 }
 
 // Largest cluster (<= 16 blocks) of this kernel with this much shared memory
