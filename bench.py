@@ -43,6 +43,8 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--e2e-steps", type=int, default=100)
+    p.add_argument("--e2e-lanes", type=int, default=2,
+                   help="independent buffer sets the end-to-end steps alternate between")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="CPU work for the oracle baseline (0 disables it)")
     p.add_argument("--no-clocks", action="store_true")
@@ -445,53 +447,83 @@ def run_ours(args):
 
 
 def run_e2e(args, w, dims, inp_cpu, b, dev, stream, flush, moe):
-    """Same path through the public API, inputs copied from pinned host
-    memory and the combined output copied back inside the timed region."""
+    """Same path through the public API with host buffers: every step copies
+    its inputs from pinned host memory, runs the four calls and copies `out`
+    back, all inside the timed region.
+
+    Steps alternate between `--e2e-lanes` independent sets of device buffers
+    and streams, so one step's copies overlap another step's kernels (a
+    serving pipeline; the copy engines and the SMs work at the same time).
+    The value is steps / time from the first step's start to the last step's
+    end.  A single-lane run (no overlap) is timed too and reported beside it.
+    """
     import torch
     h_logits = inp_cpu.logits.pin_memory()
     h_bias = None if inp_cpu.bias is None else inp_cpu.bias.pin_memory()
     h_x = inp_cpu.x.pin_memory()
     h_xs = None if inp_cpu.x_scales is None else inp_cpu.x_scales.pin_memory()
-    h_out = torch.empty(b.out.shape, dtype=b.out.dtype).pin_memory()
-    d_logits = torch.empty_like(h_logits, device=dev)
-    d_bias = None if h_bias is None else torch.empty_like(h_bias, device=dev)
-    d_x = torch.empty_like(h_x, device=dev)
-    d_xs = None if h_xs is None else torch.empty_like(h_xs, device=dev)
     h2d = sum(t.numel() * t.element_size() for t in (h_logits, h_bias, h_x, h_xs) if t is not None)
-    d2h = h_out.numel() * h_out.element_size()
 
-    def one(e0, e1):
-        e0.record(stream)
-        d_logits.copy_(h_logits, non_blocking=True)
-        if d_bias is not None:
-            d_bias.copy_(h_bias, non_blocking=True)
-        d_x.copy_(h_x, non_blocking=True)
-        if d_xs is not None:
-            d_xs.copy_(h_xs, non_blocking=True)
-        moe.route_topk(dims, d_logits, d_bias, w.score_fn, w.renormalize, b.topk_idx, b.topk_w,
-                       stream)
-        moe.dispatch_count(dims, b.topk_idx, b.expert_counts, b.expert_offsets, b.rank_counts,
-                           b.rank_offsets, b.send_counts, b.pos, b.status, stream)
-        moe.dispatch_pack(dims, d_x, d_xs, b.pos, b.packed_x, b.packed_scales, b.packed_src,
-                          stream)
-        moe.combine(dims, b.y, b.pos, b.topk_w, b.out, stream)
-        h_out.copy_(b.out, non_blocking=True)
-        e1.record(stream)
+    class Lane:
+        def __init__(self, bufs, strm):
+            self.b = bufs
+            self.s = strm
+            self.logits = torch.empty_like(h_logits, device=dev)
+            self.bias = None if h_bias is None else torch.empty_like(h_bias, device=dev)
+            self.x = torch.empty_like(h_x, device=dev)
+            self.xs = None if h_xs is None else torch.empty_like(h_xs, device=dev)
+            self.out = torch.empty(bufs.out.shape, dtype=bufs.out.dtype).pin_memory()
+
+    def one(L):
+        with torch.cuda.stream(L.s):
+            L.logits.copy_(h_logits, non_blocking=True)
+            if L.bias is not None:
+                L.bias.copy_(h_bias, non_blocking=True)
+            L.x.copy_(h_x, non_blocking=True)
+            if L.xs is not None:
+                L.xs.copy_(h_xs, non_blocking=True)
+            bb = L.b
+            moe.route_topk(dims, L.logits, L.bias, w.score_fn, w.renormalize, bb.topk_idx,
+                           bb.topk_w, L.s)
+            moe.dispatch_count(dims, bb.topk_idx, bb.expert_counts, bb.expert_offsets,
+                               bb.rank_counts, bb.rank_offsets, bb.send_counts, bb.pos,
+                               bb.status, L.s)
+            moe.dispatch_pack(dims, L.x, L.xs, bb.pos, bb.packed_x, bb.packed_scales,
+                              bb.packed_src, L.s)
+            moe.combine(dims, bb.y, bb.pos, bb.topk_w, bb.out, L.s)
+            L.out.copy_(bb.out, non_blocking=True)
+
+    def timed(lanes, n):
+        for i in range(2 * len(lanes)):
+            one(lanes[i % len(lanes)])
+        torch.cuda.synchronize(dev)
+        flush()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for L in lanes:
+            L.s.wait_event(t0)
+        for i in range(n):
+            one(lanes[i % len(lanes)])
+        for L in lanes:
+            stream.wait_stream(L.s)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        return t0.elapsed_time(t1) / n
 
     n = max(1, args.e2e_steps)
-    for _ in range(3):
-        flush()
-        one(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(n)]
-    torch.cuda.synchronize(dev)
-    for e0, e1 in evs:
-        flush()
-        one(e0, e1)
-    torch.cuda.synchronize(dev)
-    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+    lanes = [Lane(b, torch.cuda.Stream(dev))]
+    serial_ms = timed(lanes, n)
+    for _ in range(max(1, args.e2e_lanes) - 1):
+        lanes.append(Lane(moe.Buffers(dims, device=dev,
+                                      separate_y=False if w.x_dtype == w.y_dtype else None),
+                          torch.cuda.Stream(dev)))
+    ms = timed(lanes, n) if len(lanes) > 1 else serial_ms
+    d2h = lanes[0].out.numel() * lanes[0].out.element_size()
     return {"value": w.NT / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "lanes": len(lanes), "serial_ms_per_step": serial_ms,
+            "serial_value": w.NT / (serial_ms / 1e3)}
 
 
 def main():

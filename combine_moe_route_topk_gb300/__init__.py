@@ -110,10 +110,21 @@ def dims_of(w) -> MoeDims:
     return make_dims(w.N, w.T, w.E, w.R, w.H, w.x_dtype, w.y_dtype, w.cap_rows)
 
 
+_sizes_cache: dict = {}
+
+
 def buffer_sizes(dims: MoeDims) -> dict:
+    """Buffer sizes for ``dims`` (memoised: the query is pure host arithmetic)."""
+    key = bytes(dims)
+    hit = _sizes_cache.get(key)
+    if hit is not None:
+        return hit
     s = MoeSizes()
     _check(lib().moe_buffer_sizes(ctypes.byref(dims), ctypes.byref(s)))
-    return s.as_dict()
+    d = s.as_dict()
+    if len(_sizes_cache) < 256:
+        _sizes_cache[key] = d
+    return d
 
 
 def _stream(stream) -> ctypes.c_void_p:

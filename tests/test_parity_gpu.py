@@ -196,3 +196,42 @@ def test_repeated_calls_are_deterministic():
     np.testing.assert_array_equal(sa, sb)
     oa, ob = a.combine().cpu(), b.combine().cpu()
     assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
+
+
+def test_cuda_graph_capture_and_replay():
+    """The four calls capture into one CUDA graph (fixed grids, no host
+    synchronisation) and the replay recomputes everything for new inputs."""
+    import combine_moe_route_topk_gb300 as moe
+    w = W.WORKLOADS["tiny"]
+    dims = moe.dims_of(w)
+    b = moe.Buffers(dims)
+    inp = W.make_inputs(w, device="cuda")
+    logits, x = inp.logits.clone(), inp.x.clone()
+
+    def calls():
+        moe.route_topk(dims, logits, None, w.score_fn, w.renormalize, b.topk_idx, b.topk_w)
+        moe.dispatch_count(dims, b.topk_idx, b.expert_counts, b.expert_offsets, b.rank_counts,
+                           b.rank_offsets, b.send_counts, b.pos, b.status)
+        moe.dispatch_pack(dims, x, None, b.pos, b.packed_x, None, b.packed_src)
+        moe.combine(dims, b.y, b.pos, b.topk_w, b.out)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        calls()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        calls()
+    w2 = w.replace(seed=99)
+    inp2 = W.make_inputs(w2)
+    logits.copy_(inp2.logits)
+    x.copy_(inp2.x)
+    b.out.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert moe.read_status(b.status) == moe.MOE_OK
+    ref = oracle.run(w2, inp2)
+    np.testing.assert_array_equal(b.topk_idx.cpu().numpy(), ref["topk_idx"])
+    np.testing.assert_array_equal(b.pos.cpu().numpy(), ref["pos"])
+    check_combine(w2, b.out, ref["out"], ref["mag"])
