@@ -56,6 +56,9 @@ def _load():
             lib.oracle_combine.argtypes = [i64, i32, i64, i32, i64, P, P, P, P, P, P]
             lib.oracle_fp8e4m3_decode.argtypes = [ctypes.c_uint8]
             lib.oracle_fp8e4m3_decode.restype = ctypes.c_double
+            lib.oracle_f32_to_fp8e4m3.argtypes = [ctypes.c_float]
+            lib.oracle_f32_to_fp8e4m3.restype = ctypes.c_uint8
+            lib.oracle_quantize_rows.argtypes = [i64, i64, P, P, P]
             lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
             lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
             _lib = lib
@@ -151,6 +154,27 @@ def combine(y, y_dtype, pos, rank_offsets, topk_w, cap, H):
 
 def fp8e4m3_decode(code: int) -> float:
     return _load().oracle_fp8e4m3_decode(code)
+
+
+def f32_to_fp8e4m3(v: float) -> int:
+    return _load().oracle_f32_to_fp8e4m3(v)
+
+
+def quantize_rows(x_bf16_rows):
+    """Block fp8 quantisation of bf16 rows (uint16 bits or a bf16 tensor):
+    returns (codes uint8 [rows, H], scales f32 [rows, H/128])."""
+    lib = _load()
+    if hasattr(x_bf16_rows, "numpy"):
+        import torch
+        x_bf16_rows = x_bf16_rows.contiguous().view(torch.int16).numpy().view(np.uint16)
+    x = np.ascontiguousarray(x_bf16_rows, dtype=np.uint16)
+    rows, H = x.shape
+    codes = np.empty((rows, H), np.uint8)
+    scales = np.empty((rows, H // 128), np.float32)
+    rc = lib.oracle_quantize_rows(rows, H, _p(x), _p(codes), _p(scales))
+    if rc != OK:
+        raise ValueError("H must be a multiple of 128")
+    return codes, scales
 
 
 def f32_to_bf16_bits(v: float) -> int:

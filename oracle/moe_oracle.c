@@ -74,6 +74,70 @@ static double fp8e4m3_to_double(uint8_t b) {
 }
 
 double oracle_fp8e4m3_decode(uint8_t b) { return fp8e4m3_to_double(b); }
+
+/* binary32 -> e4m3, round to nearest with ties to the even code, saturating
+ * at +-448: the code whose value is nearest to v (all 127 finite magnitudes
+ * sorted ascending, found by bisection); a tie between two codes goes to
+ * the one with mantissa lsb 0; magnitudes above 448 give 448.  The sign bit
+ * is copied from v (so -0 and small negatives give 0x80).  v must not be
+ * NaN. */
+static uint8_t f32_to_fp8e4m3(float v) {
+    static double mag[127];
+    static int init = 0;
+    if (!init) {
+        for (int c = 0; c < 127; ++c) mag[c] = fp8e4m3_to_double((uint8_t)c);
+        init = 1;
+    }
+    const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    const double a = fabs((double)v);
+    if (a >= mag[126]) return (uint8_t)(sign | 126);
+    int lo = 0, hi = 126; /* mag[lo] <= a < mag[hi] */
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if (mag[mid] <= a) lo = mid;
+        else hi = mid;
+    }
+    const double dlo = a - mag[lo], dhi = mag[hi] - a;
+    int c;
+    if (dlo < dhi) c = lo;
+    else if (dhi < dlo) c = hi;
+    else c = (lo % 2 == 0) ? lo : hi;
+    return (uint8_t)(sign | c);
+}
+
+uint8_t oracle_f32_to_fp8e4m3(float v) { return f32_to_fp8e4m3(v); }
+
+/* ------------------------------------------------------------------------ */
+/* next step: fp8 block quantisation of dispatched rows  ([P1] Quantization:
+ * activations are quantised on the fly with one scaling factor per
+ * 128-element vector; [P2] Dispatch: the message carries the block scaling
+ * factors with the activations)
+ *
+ * For each row and each block of 128 consecutive elements:
+ *   amax  = max |x| over the block (bf16 values are exact in float)
+ *   scale = fl32(amax / 448)              (448: largest e4m3 value)
+ *   code  = e4m3_RNE_sat(fl32(x / scale)), or 0 when amax == 0
+ * ------------------------------------------------------------------------ */
+int oracle_quantize_rows(int64_t rows, int64_t H, const uint16_t *x_bf16, uint8_t *codes,
+                         float *scales) {
+    if (H % 128 != 0) return OR_ERR_INVALID;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b0 = 0; b0 < H; b0 += 128) {
+            float amax = 0.0f;
+            for (int64_t h = b0; h < b0 + 128; ++h) {
+                float a = fabsf(bf16_to_f32(x_bf16[r * H + h]));
+                if (a > amax) amax = a;
+            }
+            float scale = amax / 448.0f;
+            scales[r * (H / 128) + b0 / 128] = scale;
+            for (int64_t h = b0; h < b0 + 128; ++h) {
+                float v = bf16_to_f32(x_bf16[r * H + h]);
+                codes[r * H + h] = (amax == 0.0f) ? (uint8_t)0 : f32_to_fp8e4m3(v / scale);
+            }
+        }
+    }
+    return OR_OK;
+}
 uint16_t oracle_f32_to_bf16(float f) { return f32_to_bf16(f); }
 
 /* ------------------------------------------------------------------------ */

@@ -362,3 +362,59 @@ def test_dequant_expert_matches_library_decode():
     sc = inp.x_scales[torch.from_numpy(g)].repeat_interleave(128, dim=1)
     want = (q * sc).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     np.testing.assert_array_equal(r["y"], want)
+
+
+# --------------------------------------------------------------------------
+# fp8 block quantisation (fused into the quantising pack)
+# --------------------------------------------------------------------------
+
+def _e4m3_magnitudes():
+    return np.array([oracle.fp8e4m3_decode(c) for c in range(127)])
+
+
+def test_e4m3_encode_is_nearest_code_ties_to_even():
+    mags = _e4m3_magnitudes()
+    rng = np.random.default_rng(3)
+    vals = np.concatenate([rng.normal(0, 50, 3000), rng.normal(0, 0.01, 2000),
+                           (mags[1:] + mags[:-1]) / 2,            # exact midpoints
+                           -(mags[1:] + mags[:-1]) / 2, mags, -mags,
+                           [0.0, -0.0, 447.9, 448.0, 460.0, 470.0, 1e6, -1e6]]).astype(np.float32)
+    for v in vals.tolist():
+        c = oracle.f32_to_fp8e4m3(v)
+        a = abs(v)
+        if a > 448:
+            assert c & 0x7F == 126
+        else:
+            d = np.abs(mags - a)
+            best = np.flatnonzero(d == d.min())
+            want = best[0] if len(best) == 1 else [b for b in best if b % 2 == 0][0]
+            assert c & 0x7F == want, (v, c, want)
+        assert (c >> 7) == (1 if np.signbit(np.float32(v)) else 0)
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    g = torch.Generator().manual_seed(5)
+    v = torch.cat([torch.randn(20000, generator=g) * 30, torch.randn(5000, generator=g) * 1e-2])
+    v = v.clamp(-448, 448)
+    ref = v.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.f32_to_fp8e4m3(float(t)) for t in v.tolist()], np.uint8)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_block_quantisation_properties():
+    g = torch.Generator().manual_seed(7)
+    x = (torch.randn(6, 512, generator=g) * torch.tensor([1.0, 1e-3, 30.0, 0.0]).repeat_interleave(128)).to(torch.bfloat16)
+    codes, scales = oracle.quantize_rows(x)
+    xf = x.to(torch.float64).numpy().reshape(6, 4, 128)
+    amax = np.abs(xf).max(axis=2)
+    np.testing.assert_array_equal(scales, (amax.astype(np.float32) / np.float32(448)))
+    dec = np.vectorize(oracle.fp8e4m3_decode)(codes).reshape(6, 4, 128)
+    for r in range(6):
+        for blk in range(4):
+            if amax[r, blk] == 0:
+                assert (codes.reshape(6, 4, 128)[r, blk] == 0).all() and scales[r, blk] == 0
+                continue
+            # the largest element lands on +-448; the rest within half a code step
+            assert np.abs(dec[r, blk]).max() == 448.0
+            err = np.abs(dec[r, blk] * scales[r, blk] - xf[r, blk])
+            assert (err <= np.abs(xf[r, blk]) * 2.0 ** -4 + scales[r, blk] * 2.0 ** -10 + 1e-30).all()
