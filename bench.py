@@ -395,6 +395,30 @@ def run_ours(args):
     per_timed = {"dispatch (route+count+pack)": statistics.mean(dispatch_ms),
                  "combine": statistics.mean(combine_ms)}
 
+    # the quantising pack (bf16 rows -> e4m3 + per-128 scales), timed alone
+    # on the same routing; it replaces pack when the experts take fp8 input
+    quant = None
+    if w.x_dtype == W.BF16 and w.H % 128 == 0:
+        qs = moe.buffer_sizes(moe.fp8_dims(dims))
+        pq = torch.empty(qs["packed_x_bytes"], dtype=torch.uint8, device=dev)
+        ps = torch.empty(qs["packed_scales_bytes"] // 4, dtype=torch.float32, device=dev)
+        qms = []
+        for i in range(nb + 3):
+            flush()
+            e0, e1 = new_events(2)
+            e0.record(stream)
+            moe.dispatch_pack_quant(dims, inp.x, b.pos, pq, ps, b.packed_src, stream)
+            e1.record(stream)
+            if i >= 3:
+                qms.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        qm = statistics.mean(a.elapsed_time(c) for a, c in qms)
+        qbytes = w.NT * (2 * w.H + w.R * (w.H + 4 * (w.H // 128))) + w.NT * w.R * 8
+        quant = {"ms": qm, "alg_bytes": qbytes, "alg_gbs": qbytes / (qm / 1e3) / 1e9,
+                 "frac": qbytes / (qm / 1e3) / 1e9 / measured_peaks()[0],
+                 "note": "moe_dispatch_pack_quant on the same routing, timed alone"}
+        del pq, ps
+
     # ---- end to end through the public API with host buffers -------------
     e2e = run_e2e(args, w, dims, inp_cpu, b, dev, stream, flush, moe)
 
@@ -436,6 +460,7 @@ def run_ours(args):
         "pack_plus_combine": {"ms": pc_ms, "alg_gbs": pc_gbs, "frac": pc_gbs / peak,
                               "frac_of_8tbs_nominal": pc_gbs / 8000.0},
         "timed_segments_ms": per_timed,
+        "pack_quant": quant,
         "kernels": kern,
         "e2e": e2e,
         "cpu_baseline": cpu,

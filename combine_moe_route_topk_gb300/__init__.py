@@ -85,12 +85,14 @@ def lib() -> ctypes.CDLL:
             L.moe_dispatch_count.argtypes = [D, P, P, P, P, P, P, P, P, P]
             L.moe_dispatch_pack.argtypes = [D, P, P, P, P, P, P, P]
             L.moe_combine.argtypes = [D, P, P, P, P, P]
+            L.moe_dispatch_pack_quant.argtypes = [D, P, P, P, P, P, P]
             L.moe_read_status.argtypes = [P, P]
             L.moe_last_error.restype = ctypes.c_char_p
             L.moe_last_error.argtypes = []
             L.moe_version.restype = i32
             for fn in ("moe_buffer_sizes", "moe_route_topk", "moe_dispatch_count",
-                       "moe_dispatch_pack", "moe_combine", "moe_read_status"):
+                       "moe_dispatch_pack", "moe_dispatch_pack_quant", "moe_combine",
+                       "moe_read_status"):
                 getattr(L, fn).restype = i32
             _lib = L
     return _lib
@@ -186,6 +188,25 @@ def dispatch_pack(dims: MoeDims, x, x_scales, pos, packed_x, packed_scales, pack
         _ptr(packed_x, s["packed_x_bytes"], "packed_x", _TORCH_DTYPE[dims.x_dtype]),
         _ptr(packed_scales, s["packed_scales_bytes"], "packed_scales", torch.float32,
              optional=not fp8),
+        _ptr(packed_src, s["packed_src_bytes"], "packed_src", torch.int32), _stream(stream)))
+
+
+def fp8_dims(dims: MoeDims) -> MoeDims:
+    """The same problem with fp8 block-scaled rows (sizes of quantised buffers)."""
+    return make_dims(dims.N, dims.T, dims.E, dims.R, dims.H, MOE_FP8E4M3_BLK128, dims.y_dtype,
+                     dims.cap_rows)
+
+
+def dispatch_pack_quant(dims: MoeDims, x, pos, packed_q, packed_scales, packed_src,
+                        stream=None):
+    """Pack bf16 rows as e4m3 codes + one f32 scale per 128 elements."""
+    s = buffer_sizes(dims)
+    q = buffer_sizes(fp8_dims(dims))
+    _check(lib().moe_dispatch_pack_quant(
+        ctypes.byref(dims), _ptr(x, s["x_bytes"], "x", torch.bfloat16),
+        _ptr(pos, s["pos_bytes"], "pos", torch.int32),
+        _ptr(packed_q, q["packed_x_bytes"], "packed_q", torch.uint8),
+        _ptr(packed_scales, q["packed_scales_bytes"], "packed_scales", torch.float32),
         _ptr(packed_src, s["packed_src_bytes"], "packed_src", torch.int32), _stream(stream)))
 
 

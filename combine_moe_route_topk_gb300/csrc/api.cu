@@ -203,6 +203,27 @@ int moe_dispatch_pack(const MoeDims *dims, const void *x, const float *x_scales,
                        "moe_dispatch_pack");
 }
 
+int moe_dispatch_pack_quant(const MoeDims *dims, const void *x, const int32_t *pos, void *packed_q,
+                            float *packed_scales, int32_t *packed_src, void *stream) {
+    Derived v;
+    int rc = check_dims(dims, &v, "moe_dispatch_pack_quant");
+    if (rc != MOE_OK) return rc;
+    if (dims->x_dtype != MOE_BF16)
+        return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_pack_quant: x_dtype must be MOE_BF16 (the rows it reads)");
+    if (dims->H % 128 != 0)
+        return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_pack_quant: H=%d must be a multiple of 128", dims->H);
+    if (v.NT == 0) return MOE_OK;
+    if (!x || !pos || !packed_q || !packed_scales || !packed_src)
+        return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_pack_quant: a required pointer is NULL");
+    if (!aligned(x, 16) || !aligned(packed_q, 16))
+        return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_pack_quant: x and packed_q must be 16-byte aligned");
+    if (!aligned(pos, 4) || !aligned(packed_scales, 4) || !aligned(packed_src, 4))
+        return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_pack_quant: pos, packed_scales and packed_src must be 4-byte aligned");
+    return cuda_result(launch_dispatch_pack_quant(x, pos, v.NT, dims->R, dims->H, v.rows_total, packed_q,
+                                                  packed_scales, packed_src, (cudaStream_t)stream),
+                       "moe_dispatch_pack_quant");
+}
+
 int moe_combine(const MoeDims *dims, const void *y, const int32_t *pos, const float *topk_w, void *out,
                 void *stream) {
     Derived v;

@@ -32,6 +32,10 @@ cudaError_t launch_dispatch_pack(const void *x, const float *x_scales, const int
                                  int64_t rows_total, void *packed_x, float *packed_scales,
                                  int32_t *packed_src, cudaStream_t stream);
 
+cudaError_t launch_dispatch_pack_quant(const void *x, const int32_t *pos, int64_t NT, int R, int H,
+                                       int64_t rows_total, void *packed_q, float *packed_scales,
+                                       int32_t *packed_src, cudaStream_t stream);
+
 cudaError_t launch_combine(const void *y, int y_dtype, const int32_t *pos, const float *topk_w,
                            int64_t NT, int R, int H, int64_t rows_total, void *out,
                            cudaStream_t stream);

@@ -157,6 +157,28 @@ int moe_dispatch_pack(const MoeDims *dims, const void *x, const float *x_scales,
                       const int32_t *pos, void *packed_x, float *packed_scales,
                       int32_t *packed_src, void *stream);
 
+/* Dispatch pack with fp8 block quantisation fused in.  Source: "Lower
+ * latency and higher throughput with multi-node DeepSeek deployment",
+ * section "Quantization" (activations quantised on the fly, one scaling
+ * factor per 128-element vector); "Efficient and portable mixture-of-experts
+ * communication", section "Dispatch" (the message carries the activations
+ * and their block scales).
+ *   dims          x_dtype must be MOE_BF16 (the rows read); H % 128 == 0
+ *   x             bf16 [N*T][H] (in)
+ *   pos           i32 [N*T][R] from moe_dispatch_count
+ *   packed_q      u8 [N*cap][H] (out): e4m3 codes of x[g] at row pos[g][k]
+ *   packed_scales f32 [N*cap][H/128] (out): the block scales of that row
+ *   packed_src    i32 [N*cap] (out): row pos[g][k] = g*R + k
+ * Per 128-element block of a row: amax = max |x|; scale = fl32(amax/448);
+ * code = e4m3 (sign, 4-bit exponent with bias 7, 3-bit mantissa; no
+ * infinities; largest value 448) of fl32(x/scale), rounded to nearest with
+ * ties to even and saturated at +-448; amax == 0 gives scale 0 and codes 0.
+ * The packed buffers have the sizes moe_buffer_sizes reports for the same
+ * dims with x_dtype = MOE_FP8E4M3_BLK128.  NaN or infinite inputs give
+ * unspecified codes.  Rows are skipped like in moe_dispatch_pack. */
+int moe_dispatch_pack_quant(const MoeDims *dims, const void *x, const int32_t *pos, void *packed_q,
+                            float *packed_scales, int32_t *packed_src, void *stream);
+
 /* Combine.  Source: "Efficient and portable mixture-of-experts
  * communication", section "Combine" (each token reads its experts' outputs
  * through the routing table and forms their router-weighted average);

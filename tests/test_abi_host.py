@@ -104,6 +104,17 @@ def test_bad_dims_are_rejected_on_the_host(lib, kw, code, msg):
     assert lib.moe_combine(ctypes.byref(d), fake, fake, fake, fake, None) == code
 
 
+def test_quant_pack_rejects_non_bf16_rows_and_bad_h(lib):
+    P = ctypes.c_void_p
+    ok = P(0x10000)
+    d = moe.make_dims(4, 8, 16, 2, 128, x_dtype=moe.MOE_F32)
+    assert lib.moe_dispatch_pack_quant(ctypes.byref(d), ok, ok, ok, ok, ok, None) == moe.MOE_ERR_INVALID_ARG
+    assert "MOE_BF16" in lib.moe_last_error().decode()
+    d = moe.make_dims(4, 8, 16, 2, 64)
+    assert lib.moe_dispatch_pack_quant(ctypes.byref(d), ok, ok, ok, ok, ok, None) == moe.MOE_ERR_INVALID_ARG
+    assert "128" in lib.moe_last_error().decode()
+
+
 def test_reserved_field_must_be_zero(lib):
     d = moe.make_dims(4, 8, 16, 2, 64)
     d.reserved = 1

@@ -1,0 +1,93 @@
+"""Parity of the quantising pack (bf16 rows -> e4m3 codes + per-128 scales)
+with the oracle: codes, scales and packed_src bit-exact on the occupied rows.
+
+Both sides take every rounding decision in the same precision: amax is exact,
+scale = fl32(amax / 448), the quotient fl32(x / scale) is IEEE-rounded on
+both sides, and the e4m3 rounding (nearest, ties to even, saturating) is the
+format's; the oracle's encoder is pinned in test_oracle_pins.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import combine_moe_route_topk_gb300 as moe
+import oracle
+from combine_moe_route_topk_gb300 import workloads as W
+from gpu_path import compact_of_region, occupied_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from combine_moe_route_topk_gb300 import _build
+    _build.build()
+
+
+def _run(w, inp, special=None):
+    dims = moe.dims_of(w)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    b = moe.Buffers(dims, device=dev)
+    logits = inp.logits.to(dev)
+    bias = None if inp.bias is None else inp.bias.to(dev)
+    x = inp.x.to(dev)
+    q = moe.buffer_sizes(moe.fp8_dims(dims))
+    packed_q = torch.empty(q["packed_x_bytes"], dtype=torch.uint8, device=dev)
+    packed_scales = torch.empty(q["packed_scales_bytes"] // 4, dtype=torch.float32, device=dev)
+    moe.route_topk(dims, logits, bias, w.score_fn, w.renormalize, b.topk_idx, b.topk_w)
+    moe.dispatch_count(dims, b.topk_idx, b.expert_counts, b.expert_offsets, b.rank_counts,
+                       b.rank_offsets, b.send_counts, b.pos, b.status)
+    moe.dispatch_pack_quant(dims, x, b.pos, packed_q, packed_scales, b.packed_src)
+    assert moe.read_status(b.status) == moe.MOE_OK
+    cap = b.sizes["cap_rows"]
+    rank_counts = b.rank_counts.cpu().numpy()
+    rows = occupied_rows(rank_counts, cap)
+    rows_t = torch.from_numpy(rows).to(dev)
+    gq = packed_q.view(-1, w.H)[rows_t].cpu().numpy()
+    gs = packed_scales.view(-1, w.H // 128)[rows_t].cpu().numpy()
+    gsrc = b.packed_src[rows_t].cpu().numpy()
+    # oracle: quantise every token row, then pack the fp8 rows
+    idx, _, _ = oracle.route(inp.logits.numpy(), None if inp.bias is None else inp.bias.numpy(),
+                             w.R, w.score_fn, w.renormalize)
+    cnt, st = oracle.count(w.N, w.T, w.E, cap, idx)
+    assert st == oracle.OK
+    codes, scales = oracle.quantize_rows(inp.x)
+    oq, osc, osrc = oracle.pack(codes, scales, cnt["pos"], cnt["rank_offsets"], cap)
+    crow = compact_of_region(rows, cap, cnt["rank_offsets"])
+    np.testing.assert_array_equal(gsrc, osrc[crow])
+    np.testing.assert_array_equal(gs.view(np.uint32), osc[crow].view(np.uint32))
+    bad = np.argwhere(gq != oq[crow])
+    assert bad.size == 0, (f"{len(bad)} codes differ, first at {tuple(bad[0])}: "
+                           f"got {gq[tuple(bad[0])]:#04x} want {oq[crow][tuple(bad[0])]:#04x}")
+
+
+def test_quant_pack_full_size_dsv3():
+    w = W.WORKLOADS["dsv3_decode"]
+    _run(w, W.make_inputs(w))
+
+
+def test_quant_pack_full_size_kimi():
+    w = W.WORKLOADS["kimi_k2_decode"]
+    _run(w, W.make_inputs(w))
+
+
+@pytest.mark.parametrize("N,T,E,R,H", [(3, 77, 24, 3, 128), (4, 50, 32, 5, 384),
+                                       (2, 300, 16, 2, 1152)])
+def test_quant_pack_ragged(N, T, E, R, H):
+    w = W.Workload("q", N=N, T=T, E=E, R=R, H=H, seed=N * T)
+    _run(w, W.make_inputs(w))
+
+
+def test_quant_pack_zero_blocks_tiny_values_and_signed_zeros():
+    w = W.Workload("qz", N=2, T=64, E=8, R=2, H=512, seed=31)
+    inp = W.make_inputs(w)
+    x = inp.x.to(torch.float32)
+    x[:, 0:128] = 0.0                       # all-zero block: scale 0, codes 0
+    x[::2, 128:256] *= 1e-30                # tiny values (still bf16 normals/subnormals)
+    x[1::2, 256:384] = -0.0                 # negative zeros next to normal values
+    x[1::2, 300] = 3.0
+    x[:, 384] = 1e-6                        # underflows to a zero code after scaling
+    x[:, 385] = -1e-6
+    x[:, 386] = 50.0
+    inp.x = x.to(torch.bfloat16)
+    _run(w, inp)
