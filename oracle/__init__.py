@@ -59,6 +59,9 @@ def _load():
             lib.oracle_f32_to_fp8e4m3.argtypes = [ctypes.c_float]
             lib.oracle_f32_to_fp8e4m3.restype = ctypes.c_uint8
             lib.oracle_quantize_rows.argtypes = [i64, i64, P, P, P]
+            lib.oracle_combine_rank.argtypes = [i64, i32, i64, i32, i64, i32, P, P, P, P, P]
+            lib.oracle_combine_partials.argtypes = [i64, i32, i32, i64, i32, i64, P, P, P, P, P, P]
+            lib.oracle_reduce_partials.argtypes = [i64, i32, i64, i32, P, P, P]
             lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
             lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
             _lib = lib
@@ -150,6 +153,43 @@ def combine(y, y_dtype, pos, rank_offsets, topk_w, cap, H):
     lib.oracle_combine(NT, R, H, y_dtype, cap, _p(y), _p(pos), _p(_c(rank_offsets, np.int32)),
                        _p(_c(topk_w, np.float32)), _p(out), _p(mag))
     return out, mag
+
+
+def combine_rank(y, y_dtype, pos, rank_offsets, topk_w, cap, H, rank):
+    """Local accumulation of one rank: sum of w*y over the token's pairs on
+    `rank` (0 where there are none), in double."""
+    lib = _load()
+    pos = _c(pos, np.int32)
+    NT, R = pos.shape
+    out = np.empty((NT, H), np.float64)
+    lib.oracle_combine_rank(NT, R, H, y_dtype, cap, rank, _p(np.ascontiguousarray(y)), _p(pos),
+                            _p(_c(rank_offsets, np.int32)), _p(_c(topk_w, np.float32)), _p(out))
+    return out
+
+
+def combine_partials(y, y_dtype, pos, rank_offsets, topk_w, cap, H, N):
+    """Per (token, distinct destination rank) partial rows rounded to y_dtype.
+    Returns (partial [NT, P, H], slot_rank i32 [NT, P]) with P = min(R, N)."""
+    lib = _load()
+    pos = _c(pos, np.int32)
+    NT, R = pos.shape
+    P = min(R, N)
+    partial = np.zeros((NT, P, H), np.uint16 if y_dtype == BF16 else np.float32)
+    slot_rank = np.empty((NT, P), np.int32)
+    lib.oracle_combine_partials(NT, R, P, H, y_dtype, cap, _p(np.ascontiguousarray(y)), _p(pos),
+                                _p(_c(rank_offsets, np.int32)), _p(_c(topk_w, np.float32)),
+                                _p(partial), _p(slot_rank))
+    return partial, slot_rank
+
+
+def reduce_partials(partial, slot_rank, y_dtype):
+    """out[g] = sum of the used partial rows of token g, in double."""
+    lib = _load()
+    NT, P, H = partial.shape
+    out = np.empty((NT, H), np.float64)
+    lib.oracle_reduce_partials(NT, P, H, y_dtype, _p(np.ascontiguousarray(partial)),
+                               _p(_c(slot_rank, np.int32)), _p(out))
+    return out
 
 
 def fp8e4m3_decode(code: int) -> float:

@@ -395,3 +395,104 @@ int oracle_combine(int64_t NT, int R, int64_t H, int y_dtype, int64_t cap, const
     }
     return OR_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* next steps: accumulation of a token's pairs per destination rank
+ * ([P5] Evaluation: accumulating on the send side reduces the data moved,
+ * at some cost in accuracy; [P4] Expert parallel: with replicated inputs a
+ * rank handles only the tokens routed to its own experts and accumulates
+ * locally before an all-reduce)
+ *
+ * The rank of pair (g, k) is d = pos / cap (pairs with pos < 0 are skipped).
+ *
+ * oracle_combine_rank: out[g] = sum over pairs of g on rank `rank` of
+ *   w * y[row], in double (0 for tokens with no pair there).  Summed over
+ *   all ranks this is the combine.
+ *
+ * oracle_combine_partials: the distinct ranks of token g, in the order of
+ *   their first pair k, get slots j = 0, 1, ...; partial[g][j] = sum over
+ *   the pairs of g on that rank of w * y[row] in double, rounded to float
+ *   and then to y_dtype (the 16-bit row a rank would send back);
+ *   slot_rank[g][j] = that rank, or -1 for unused slots (zero rows); P =
+ *   min(R, N) slots per token.
+ *
+ * oracle_reduce_partials: out[g] = sum over used slots of partial[g][j], in
+ *   double.
+ * ------------------------------------------------------------------------ */
+int oracle_combine_rank(int64_t NT, int R, int64_t H, int y_dtype, int64_t cap, int rank,
+                        const void *y, const int32_t *pos, const int32_t *rank_offsets,
+                        const float *topk_w, double *out) {
+    for (int64_t g = 0; g < NT; ++g) {
+        for (int64_t h = 0; h < H; ++h) out[g * H + h] = 0.0;
+        for (int k = 0; k < R; ++k) {
+            int32_t p = pos[g * R + k];
+            if (p < 0 || p / cap != rank) continue;
+            int64_t c = compact_row(p, cap, rank_offsets);
+            double w = (double)topk_w[g * R + k];
+            for (int64_t h = 0; h < H; ++h) {
+                double v = (y_dtype == OR_BF16)
+                               ? (double)bf16_to_f32(((const uint16_t *)y)[c * H + h])
+                               : (double)((const float *)y)[c * H + h];
+                out[g * H + h] += w * v;
+            }
+        }
+    }
+    return OR_OK;
+}
+
+int oracle_combine_partials(int64_t NT, int R, int P, int64_t H, int y_dtype, int64_t cap,
+                            const void *y, const int32_t *pos, const int32_t *rank_offsets,
+                            const float *topk_w, void *partial, int32_t *slot_rank) {
+    double *acc = (double *)malloc(sizeof(double) * (size_t)H);
+    for (int64_t g = 0; g < NT; ++g) {
+        int nslot = 0;
+        for (int j = 0; j < P; ++j) slot_rank[g * P + j] = -1;
+        for (int k = 0; k < R; ++k) {
+            int32_t p = pos[g * R + k];
+            if (p < 0) continue;
+            int d = (int)(p / cap), seen = 0;
+            for (int j = 0; j < nslot; ++j)
+                if (slot_rank[g * P + j] == d) seen = 1;
+            if (!seen && nslot < P) slot_rank[g * P + nslot++] = d;
+        }
+        for (int j = 0; j < P; ++j) {
+            for (int64_t h = 0; h < H; ++h) acc[h] = 0.0;
+            for (int k = 0; k < R && j < nslot; ++k) {
+                int32_t p = pos[g * R + k];
+                if (p < 0 || p / cap != slot_rank[g * P + j]) continue;
+                int64_t c = compact_row(p, cap, rank_offsets);
+                double w = (double)topk_w[g * R + k];
+                for (int64_t h = 0; h < H; ++h) {
+                    double v = (y_dtype == OR_BF16)
+                                   ? (double)bf16_to_f32(((const uint16_t *)y)[c * H + h])
+                                   : (double)((const float *)y)[c * H + h];
+                    acc[h] += w * v;
+                }
+            }
+            for (int64_t h = 0; h < H; ++h) {
+                int64_t o = (g * P + j) * H + h;
+                if (y_dtype == OR_BF16) ((uint16_t *)partial)[o] = f32_to_bf16((float)acc[h]);
+                else ((float *)partial)[o] = (float)acc[h];
+            }
+        }
+    }
+    free(acc);
+    return OR_OK;
+}
+
+int oracle_reduce_partials(int64_t NT, int P, int64_t H, int y_dtype, const void *partial,
+                           const int32_t *slot_rank, double *out) {
+    for (int64_t g = 0; g < NT; ++g) {
+        for (int64_t h = 0; h < H; ++h) {
+            double s = 0.0;
+            for (int j = 0; j < P; ++j) {
+                if (slot_rank[g * P + j] < 0) continue;
+                int64_t o = (g * P + j) * H + h;
+                s += (y_dtype == OR_BF16) ? (double)bf16_to_f32(((const uint16_t *)partial)[o])
+                                          : (double)((const float *)partial)[o];
+            }
+            out[g * H + h] = s;
+        }
+    }
+    return OR_OK;
+}

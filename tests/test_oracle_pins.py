@@ -418,3 +418,71 @@ def test_block_quantisation_properties():
             assert np.abs(dec[r, blk]).max() == 448.0
             err = np.abs(dec[r, blk] * scales[r, blk] - xf[r, blk])
             assert (err <= np.abs(xf[r, blk]) * 2.0 ** -4 + scales[r, blk] * 2.0 ** -10 + 1e-30).all()
+
+
+# --------------------------------------------------------------------------
+# accumulation per destination rank (send-side partials, EP-only local part)
+# --------------------------------------------------------------------------
+
+def _routed(w):
+    inp = W.make_inputs(w)
+    r = oracle.run(w, inp)
+    return inp, r
+
+
+def test_rank_accumulations_sum_to_the_combine():
+    # sum over ranks of the local accumulations = the combine (closed form)
+    w = W.Workload("t", N=4, T=21, E=16, R=5, H=40, x_dtype=W.F32, y_dtype=W.F32,
+                   expert_op=W.EXPERT_SCALE, seed=23)
+    inp, r = _routed(w)
+    tot = sum(oracle.combine_rank(r["y"], w.y_dtype, r["pos"], r["rank_offsets"], r["topk_w"],
+                                  r["cap"], w.H, d) for d in range(w.N))
+    np.testing.assert_allclose(tot, r["out"], rtol=1e-13, atol=1e-300)
+
+
+def test_rank_accumulation_only_sees_local_pairs():
+    # identity expert: out_d[g] = x[g] * (sum of the weights of g's pairs on d)
+    w = W.Workload("t", N=4, T=17, E=16, R=3, H=24, x_dtype=W.F32, y_dtype=W.F32, seed=29)
+    inp, r = _routed(w)
+    L = w.E // w.N
+    xd = inp.x.to(torch.float64).numpy()
+    for d in range(w.N):
+        got = oracle.combine_rank(r["y"], w.y_dtype, r["pos"], r["rank_offsets"], r["topk_w"],
+                                  r["cap"], w.H, d)
+        wsum = (r["topk_w"].astype(np.float64) * (r["topk_idx"] // L == d)).sum(1, keepdims=True)
+        np.testing.assert_allclose(got, xd * wsum, rtol=1e-14, atol=1e-300)
+
+
+def test_partials_slots_follow_first_appearance_and_sum_to_combine():
+    w = W.Workload("t", N=4, T=19, E=32, R=6, H=32, x_dtype=W.F32, y_dtype=W.F32, seed=37)
+    inp, r = _routed(w)
+    part, slot = oracle.combine_partials(r["y"], w.y_dtype, r["pos"], r["rank_offsets"],
+                                         r["topk_w"], r["cap"], w.H, w.N)
+    L = w.E // w.N
+    for g in range(w.NT):
+        ranks = []
+        for k in range(w.R):
+            d = int(r["topk_idx"][g, k]) // L
+            if d not in ranks:
+                ranks.append(d)
+        assert slot[g].tolist() == ranks + [-1] * (min(w.R, w.N) - len(ranks))
+    out = oracle.reduce_partials(part, slot, w.y_dtype)
+    # f32 partials: each rounded once to float
+    np.testing.assert_allclose(out, r["out"], rtol=3 * 2.0 ** -24 * w.R, atol=1e-30)
+
+
+def test_bf16_partials_round_each_rank_sum_once():
+    w = W.Workload("t", N=2, T=16, E=8, R=4, H=16, seed=41)
+    inp, r = _routed(w)
+    part, slot = oracle.combine_partials(r["y"], w.y_dtype, r["pos"], r["rank_offsets"],
+                                         r["topk_w"], r["cap"], w.H, w.N)
+    for j in range(part.shape[1]):
+        for g in range(w.NT):
+            d = slot[g, j]
+            if d < 0:
+                assert (part[g, j] == 0).all()
+                continue
+            want = oracle.combine_rank(r["y"], w.y_dtype, r["pos"][g:g + 1], r["rank_offsets"],
+                                       r["topk_w"][g:g + 1], r["cap"], w.H, int(d))[0]
+            bits = np.array([oracle.f32_to_bf16_bits(float(np.float32(v))) for v in want], np.uint16)
+            np.testing.assert_array_equal(part[g, j], bits)
