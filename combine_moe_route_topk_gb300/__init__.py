@@ -54,7 +54,8 @@ _SIZE_FIELDS = ["bound_rows", "cap_rows", "total_pairs", "logits_bytes", "topk_i
                 "topk_w_bytes", "pos_bytes", "expert_counts_bytes", "expert_offsets_bytes",
                 "rank_counts_bytes", "rank_offsets_bytes", "send_counts_bytes", "x_bytes",
                 "x_scales_bytes", "packed_x_bytes", "packed_scales_bytes", "packed_src_bytes",
-                "y_bytes", "out_bytes", "status_bytes"]
+                "y_bytes", "out_bytes", "status_bytes", "partial_slots", "partial_bytes",
+                "slot_rank_bytes"]
 
 
 class MoeSizes(ctypes.Structure):
@@ -86,13 +87,18 @@ def lib() -> ctypes.CDLL:
             L.moe_dispatch_pack.argtypes = [D, P, P, P, P, P, P, P]
             L.moe_combine.argtypes = [D, P, P, P, P, P]
             L.moe_dispatch_pack_quant.argtypes = [D, P, P, P, P, P, P]
+            L.moe_dispatch_pack_rank.argtypes = [D, i32, P, P, P, P, P, P, P]
+            L.moe_combine_rank.argtypes = [D, i32, P, P, P, P, P]
+            L.moe_combine_partials.argtypes = [D, P, P, P, P, P, P]
+            L.moe_combine_reduce_partials.argtypes = [D, P, P, P, P]
             L.moe_read_status.argtypes = [P, P]
             L.moe_last_error.restype = ctypes.c_char_p
             L.moe_last_error.argtypes = []
             L.moe_version.restype = i32
             for fn in ("moe_buffer_sizes", "moe_route_topk", "moe_dispatch_count",
-                       "moe_dispatch_pack", "moe_dispatch_pack_quant", "moe_combine",
-                       "moe_read_status"):
+                       "moe_dispatch_pack", "moe_dispatch_pack_quant", "moe_dispatch_pack_rank",
+                       "moe_combine", "moe_combine_rank", "moe_combine_partials",
+                       "moe_combine_reduce_partials", "moe_read_status"):
                 getattr(L, fn).restype = i32
             _lib = L
     return _lib
@@ -217,6 +223,54 @@ def combine(dims: MoeDims, y, pos, topk_w, out, stream=None):
         ctypes.byref(dims), _ptr(y, s["y_bytes"], "y", yt),
         _ptr(pos, s["pos_bytes"], "pos", torch.int32),
         _ptr(topk_w, s["topk_w_bytes"], "topk_w", torch.float32),
+        _ptr(out, s["out_bytes"], "out", yt), _stream(stream)))
+
+
+def dispatch_pack_rank(dims: MoeDims, rank: int, x, x_scales, pos, packed_x, packed_scales,
+                       packed_src, stream=None):
+    """moe_dispatch_pack restricted to the pairs routed to rank `rank`."""
+    s = buffer_sizes(dims)
+    fp8 = dims.x_dtype == MOE_FP8E4M3_BLK128
+    _check(lib().moe_dispatch_pack_rank(
+        ctypes.byref(dims), int(rank), _ptr(x, s["x_bytes"], "x", _TORCH_DTYPE[dims.x_dtype]),
+        _ptr(x_scales, s["x_scales_bytes"], "x_scales", torch.float32, optional=not fp8),
+        _ptr(pos, s["pos_bytes"], "pos", torch.int32),
+        _ptr(packed_x, s["packed_x_bytes"], "packed_x", _TORCH_DTYPE[dims.x_dtype]),
+        _ptr(packed_scales, s["packed_scales_bytes"], "packed_scales", torch.float32,
+             optional=not fp8),
+        _ptr(packed_src, s["packed_src_bytes"], "packed_src", torch.int32), _stream(stream)))
+
+
+def combine_rank(dims: MoeDims, rank: int, y, pos, topk_w, out, stream=None):
+    """Local accumulation of rank `rank` (dense [N*T][H])."""
+    s = buffer_sizes(dims)
+    yt = _TORCH_DTYPE[dims.y_dtype]
+    _check(lib().moe_combine_rank(
+        ctypes.byref(dims), int(rank), _ptr(y, s["y_bytes"], "y", yt),
+        _ptr(pos, s["pos_bytes"], "pos", torch.int32),
+        _ptr(topk_w, s["topk_w_bytes"], "topk_w", torch.float32),
+        _ptr(out, s["out_bytes"], "out", yt), _stream(stream)))
+
+
+def combine_partials(dims: MoeDims, y, pos, topk_w, partial, slot_rank, stream=None):
+    """Per (token, destination rank) partial rows and their ranks."""
+    s = buffer_sizes(dims)
+    yt = _TORCH_DTYPE[dims.y_dtype]
+    _check(lib().moe_combine_partials(
+        ctypes.byref(dims), _ptr(y, s["y_bytes"], "y", yt),
+        _ptr(pos, s["pos_bytes"], "pos", torch.int32),
+        _ptr(topk_w, s["topk_w_bytes"], "topk_w", torch.float32),
+        _ptr(partial, s["partial_bytes"], "partial", yt),
+        _ptr(slot_rank, s["slot_rank_bytes"], "slot_rank", torch.int32), _stream(stream)))
+
+
+def combine_reduce_partials(dims: MoeDims, partial, slot_rank, out, stream=None):
+    """out[g] = sum of token g's used partial rows."""
+    s = buffer_sizes(dims)
+    yt = _TORCH_DTYPE[dims.y_dtype]
+    _check(lib().moe_combine_reduce_partials(
+        ctypes.byref(dims), _ptr(partial, s["partial_bytes"], "partial", yt),
+        _ptr(slot_rank, s["slot_rank_bytes"], "slot_rank", torch.int32),
         _ptr(out, s["out_bytes"], "out", yt), _stream(stream)))
 
 

@@ -139,6 +139,9 @@ int moe_buffer_sizes(const MoeDims *dims, MoeSizes *out) {
     out->y_bytes = v.rows_total * v.y_row_bytes;
     out->out_bytes = v.NT * v.y_row_bytes;
     out->status_bytes = 4;
+    out->partial_slots = dims->R < N ? dims->R : N;
+    out->partial_bytes = v.NT * out->partial_slots * v.y_row_bytes;
+    out->slot_rank_bytes = v.NT * out->partial_slots * 4;
     (void)H;
     return MOE_OK;
 }
@@ -197,7 +200,7 @@ int moe_dispatch_pack(const MoeDims *dims, const void *x, const float *x_scales,
     if (!aligned(pos, 4) || !aligned(packed_src, 4) || (fp8 && (!aligned(x_scales, 4) || !aligned(packed_scales, 4))))
         return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_pack: index and scale pointers must be 4-byte aligned");
     return cuda_result(launch_dispatch_pack(x, fp8 ? x_scales : nullptr, pos, v.NT, dims->R, v.x_row_bytes,
-                                            v.scales_per_row, v.rows_total, packed_x,
+                                            v.scales_per_row, 0, v.rows_total, packed_x,
                                             fp8 ? packed_scales : nullptr, packed_src,
                                             (cudaStream_t)stream),
                        "moe_dispatch_pack");
@@ -236,9 +239,86 @@ int moe_combine(const MoeDims *dims, const void *y, const int32_t *pos, const fl
         return set_error(MOE_ERR_INVALID_ARG, "moe_combine: y and out must be 16-byte aligned");
     if (!aligned(pos, 4) || !aligned(topk_w, 4))
         return set_error(MOE_ERR_INVALID_ARG, "moe_combine: pos and topk_w must be 4-byte aligned");
-    return cuda_result(launch_combine(y, dims->y_dtype, pos, topk_w, v.NT, dims->R, dims->H, v.rows_total,
+    return cuda_result(launch_combine(y, dims->y_dtype, pos, topk_w, v.NT, dims->R, dims->H, 0, v.rows_total,
                                       out, (cudaStream_t)stream),
                        "moe_combine");
+}
+
+int moe_dispatch_pack_rank(const MoeDims *dims, int rank, const void *x, const float *x_scales,
+                           const int32_t *pos, void *packed_x, float *packed_scales,
+                           int32_t *packed_src, void *stream) {
+    Derived v;
+    int rc = check_dims(dims, &v, "moe_dispatch_pack_rank");
+    if (rc != MOE_OK) return rc;
+    if (rank < 0 || rank >= dims->N)
+        return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_pack_rank: rank %d outside [0, %d)", rank, dims->N);
+    if (v.NT == 0) return MOE_OK;
+    const bool fp8 = dims->x_dtype == MOE_FP8E4M3_BLK128;
+    if (!x || !pos || !packed_x || !packed_src || (fp8 && (!x_scales || !packed_scales)))
+        return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_pack_rank: a required pointer is NULL");
+    if (!aligned(x, 16) || !aligned(packed_x, 16))
+        return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_pack_rank: x and packed_x must be 16-byte aligned");
+    if (!aligned(pos, 4) || !aligned(packed_src, 4) || (fp8 && (!aligned(x_scales, 4) || !aligned(packed_scales, 4))))
+        return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_pack_rank: index and scale pointers must be 4-byte aligned");
+    return cuda_result(launch_dispatch_pack(x, fp8 ? x_scales : nullptr, pos, v.NT, dims->R, v.x_row_bytes,
+                                            v.scales_per_row, (int64_t)rank * v.cap, (int64_t)(rank + 1) * v.cap,
+                                            packed_x, fp8 ? packed_scales : nullptr, packed_src,
+                                            (cudaStream_t)stream),
+                       "moe_dispatch_pack_rank");
+}
+
+int moe_combine_rank(const MoeDims *dims, int rank, const void *y, const int32_t *pos,
+                     const float *topk_w, void *out, void *stream) {
+    Derived v;
+    int rc = check_dims(dims, &v, "moe_combine_rank");
+    if (rc != MOE_OK) return rc;
+    if (rank < 0 || rank >= dims->N)
+        return set_error(MOE_ERR_INVALID_ARG, "moe_combine_rank: rank %d outside [0, %d)", rank, dims->N);
+    if (v.NT == 0) return MOE_OK;
+    if (!y || !pos || !topk_w || !out)
+        return set_error(MOE_ERR_INVALID_ARG, "moe_combine_rank: a required pointer is NULL");
+    if (!aligned(y, 16) || !aligned(out, 16))
+        return set_error(MOE_ERR_INVALID_ARG, "moe_combine_rank: y and out must be 16-byte aligned");
+    if (!aligned(pos, 4) || !aligned(topk_w, 4))
+        return set_error(MOE_ERR_INVALID_ARG, "moe_combine_rank: pos and topk_w must be 4-byte aligned");
+    return cuda_result(launch_combine(y, dims->y_dtype, pos, topk_w, v.NT, dims->R, dims->H,
+                                      (int64_t)rank * v.cap, (int64_t)(rank + 1) * v.cap, out,
+                                      (cudaStream_t)stream),
+                       "moe_combine_rank");
+}
+
+int moe_combine_partials(const MoeDims *dims, const void *y, const int32_t *pos,
+                         const float *topk_w, void *partial, int32_t *slot_rank, void *stream) {
+    Derived v;
+    int rc = check_dims(dims, &v, "moe_combine_partials");
+    if (rc != MOE_OK) return rc;
+    if (v.NT == 0) return MOE_OK;
+    if (!y || !pos || !topk_w || !partial || !slot_rank)
+        return set_error(MOE_ERR_INVALID_ARG, "moe_combine_partials: a required pointer is NULL");
+    if (!aligned(y, 16) || !aligned(partial, 16))
+        return set_error(MOE_ERR_INVALID_ARG, "moe_combine_partials: y and partial must be 16-byte aligned");
+    if (!aligned(pos, 4) || !aligned(topk_w, 4) || !aligned(slot_rank, 4))
+        return set_error(MOE_ERR_INVALID_ARG, "moe_combine_partials: pos, topk_w and slot_rank must be 4-byte aligned");
+    const int P = dims->R < dims->N ? dims->R : dims->N;
+    return cuda_result(launch_combine_partials(y, dims->y_dtype, pos, topk_w, v.NT, dims->R, dims->H, v.cap,
+                                               v.rows_total, P, partial, slot_rank, (cudaStream_t)stream),
+                       "moe_combine_partials");
+}
+
+int moe_combine_reduce_partials(const MoeDims *dims, const void *partial, const int32_t *slot_rank,
+                                void *out, void *stream) {
+    Derived v;
+    int rc = check_dims(dims, &v, "moe_combine_reduce_partials");
+    if (rc != MOE_OK) return rc;
+    if (v.NT == 0) return MOE_OK;
+    if (!partial || !slot_rank || !out)
+        return set_error(MOE_ERR_INVALID_ARG, "moe_combine_reduce_partials: a required pointer is NULL");
+    if (!aligned(partial, 16) || !aligned(out, 16) || !aligned(slot_rank, 4))
+        return set_error(MOE_ERR_INVALID_ARG, "moe_combine_reduce_partials: misaligned pointer");
+    const int P = dims->R < dims->N ? dims->R : dims->N;
+    return cuda_result(launch_reduce_partials(partial, dims->y_dtype, slot_rank, v.NT, P, dims->H, out,
+                                              (cudaStream_t)stream),
+                       "moe_combine_reduce_partials");
 }
 
 int moe_read_status(const int32_t *status, void *stream) {

@@ -8,6 +8,11 @@
 // contiguously per destination.  Here the destination regions are
 // partitions of one allocation, so the "send" is the packing store itself.
 //
+// Only pairs whose row lies in [row_lo, row_hi) are copied: all rank
+// regions for the dispatch, one rank's region when a rank selects the
+// tokens routed to its own experts from replicated inputs ("Hosting Qwen on
+// Blackwell", section "Expert parallel").
+//
 // The kernel is a pure HBM stream: each x row is read once and written R
 // times.  One block handles one token at a time; its threads move 16-byte
 // vectors (every row starts on a 16-byte boundary because H*elem % 16 == 0),
@@ -32,7 +37,7 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
 __global__ void __launch_bounds__(kPackThreads)
 dispatch_pack_kernel(const uint4 *__restrict__ x, const float *__restrict__ x_scales,
                      const int32_t *__restrict__ pos, int64_t NT, int R, int nvec, int spr,
-                     int64_t rows_total, uint4 *__restrict__ packed_x,
+                     int64_t row_lo, int64_t row_hi, uint4 *__restrict__ packed_x,
                      float *__restrict__ packed_scales, int32_t *__restrict__ packed_src) {
     __shared__ int s_pos[32];
     const int tid = threadIdx.x;
@@ -41,7 +46,7 @@ dispatch_pack_kernel(const uint4 *__restrict__ x, const float *__restrict__ x_sc
     for (int64_t g = blockIdx.x; g < NT; g += gridDim.x) {
         if (tid < R) {
             const int p = __ldg(pos + g * R + tid);
-            const bool ok = p >= 0 && (int64_t)p < rows_total;
+            const bool ok = (int64_t)p >= row_lo && (int64_t)p < row_hi;
             s_pos[tid] = ok ? p : -1;
             if (ok) packed_src[p] = (int32_t)(g * R + tid);
         }
@@ -80,8 +85,8 @@ dispatch_pack_kernel(const uint4 *__restrict__ x, const float *__restrict__ x_sc
 
 cudaError_t launch_dispatch_pack(const void *x, const float *x_scales, const int32_t *pos,
                                  int64_t NT, int R, int64_t row_bytes, int scales_per_row,
-                                 int64_t rows_total, void *packed_x, float *packed_scales,
-                                 int32_t *packed_src, cudaStream_t stream) {
+                                 int64_t row_lo, int64_t row_hi, void *packed_x,
+                                 float *packed_scales, int32_t *packed_src, cudaStream_t stream) {
     if (NT == 0) return cudaSuccess;
     const int nvec = (int)(row_bytes / 16);
     const int64_t grid = NT < (int64_t)0x7fffffff ? NT : (int64_t)0x7fffffff;
@@ -93,7 +98,7 @@ cudaError_t launch_dispatch_pack(const void *x, const float *x_scales, const int
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, dispatch_pack_kernel, reinterpret_cast<const uint4 *>(x),
-                              x_scales, pos, NT, R, nvec, scales_per_row, rows_total,
+                              x_scales, pos, NT, R, nvec, scales_per_row, row_lo, row_hi,
                               reinterpret_cast<uint4 *>(packed_x), packed_scales, packed_src);
 }
 

@@ -27,17 +27,27 @@ cudaError_t launch_dispatch_count(const int32_t *topk_idx, int N, int T, int E, 
                                   int32_t *send_counts, int32_t *pos, int32_t *status,
                                   cudaStream_t stream);
 
+// Pairs whose row lies outside [row_lo, row_hi) are skipped.
 cudaError_t launch_dispatch_pack(const void *x, const float *x_scales, const int32_t *pos,
                                  int64_t NT, int R, int64_t row_bytes, int scales_per_row,
-                                 int64_t rows_total, void *packed_x, float *packed_scales,
-                                 int32_t *packed_src, cudaStream_t stream);
+                                 int64_t row_lo, int64_t row_hi, void *packed_x,
+                                 float *packed_scales, int32_t *packed_src, cudaStream_t stream);
 
 cudaError_t launch_dispatch_pack_quant(const void *x, const int32_t *pos, int64_t NT, int R, int H,
                                        int64_t rows_total, void *packed_q, float *packed_scales,
                                        int32_t *packed_src, cudaStream_t stream);
 
+// Pairs whose row lies outside [row_lo, row_hi) contribute nothing.
 cudaError_t launch_combine(const void *y, int y_dtype, const int32_t *pos, const float *topk_w,
-                           int64_t NT, int R, int H, int64_t rows_total, void *out,
+                           int64_t NT, int R, int H, int64_t row_lo, int64_t row_hi, void *out,
                            cudaStream_t stream);
+
+cudaError_t launch_combine_partials(const void *y, int y_dtype, const int32_t *pos,
+                                    const float *topk_w, int64_t NT, int R, int H, int64_t cap,
+                                    int64_t rows_total, int P, void *partial, int32_t *slot_rank,
+                                    cudaStream_t stream);
+
+cudaError_t launch_reduce_partials(const void *partial, int y_dtype, const int32_t *slot_rank,
+                                   int64_t NT, int P, int H, void *out, cudaStream_t stream);
 
 }  // namespace moe

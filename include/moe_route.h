@@ -89,6 +89,9 @@ typedef struct MoeSizes {
     int64_t y_bytes;             /* [N*cap][H] of y_dtype */
     int64_t out_bytes;           /* [N*T][H] of y_dtype */
     int64_t status_bytes;        /* i32 [1] */
+    int64_t partial_slots;       /* P = min(R, N): partial rows per token */
+    int64_t partial_bytes;       /* [N*T][P][H] of y_dtype (moe_combine_partials) */
+    int64_t slot_rank_bytes;     /* i32 [N*T][P] */
 } MoeSizes;
 
 /* Fill *out with the buffer sizes for dims (host only, no CUDA call).
@@ -191,6 +194,44 @@ int moe_dispatch_pack_quant(const MoeDims *dims, const void *x, const int32_t *p
  * Pairs with pos < 0 (or outside [0, N*cap)) contribute nothing. */
 int moe_combine(const MoeDims *dims, const void *y, const int32_t *pos, const float *topk_w,
                 void *out, void *stream);
+
+/* Dispatch pack restricted to one rank (expert-parallel prefill with
+ * replicated inputs: a rank selects only the tokens routed to its own
+ * experts).  Source: "Hosting Qwen on Blackwell", section "Expert parallel".
+ * Same arguments and layout as moe_dispatch_pack; only pairs whose row lies
+ * in rank `rank`'s region [rank*cap, (rank+1)*cap) are written.
+ * 0 <= rank < N. */
+int moe_dispatch_pack_rank(const MoeDims *dims, int rank, const void *x, const float *x_scales,
+                           const int32_t *pos, void *packed_x, float *packed_scales,
+                           int32_t *packed_src, void *stream);
+
+/* Local accumulation of one rank (expert-parallel prefill: each rank sums
+ * its own experts' outputs for every token; an all-reduce over ranks, not
+ * part of this library, completes the combine).  Source: "Hosting Qwen on
+ * Blackwell", section "Expert parallel".
+ *   out [N*T][H] of y_dtype (out): out[g] = sum over the pairs of g on rank
+ *       `rank` of topk_w * y[pos], f32 accumulation in k order (0 for
+ *       tokens with no pair there).  Summed over all ranks this is
+ *       moe_combine's result up to rounding.  0 <= rank < N. */
+int moe_combine_rank(const MoeDims *dims, int rank, const void *y, const int32_t *pos,
+                     const float *topk_w, void *out, void *stream);
+
+/* Combine with send-side accumulation, first half: one partial row per
+ * (token, destination rank).  Source: "Enabling trillion-parameter models on
+ * AWS EFA", section "Evaluation" (accumulating on the send side moves less
+ * data back, with some accuracy cost).
+ *   partial   [N*T][P][H] of y_dtype (out), P = min(R, N): slot j of token g
+ *             is the j-th distinct rank of g's pairs in k order; it holds the
+ *             sum over g's pairs on that rank of topk_w * y[pos] (f32,
+ *             rounded once to y_dtype).  Unused slots are zero rows.
+ *   slot_rank i32 [N*T][P] (out): the rank of each slot, -1 if unused. */
+int moe_combine_partials(const MoeDims *dims, const void *y, const int32_t *pos,
+                         const float *topk_w, void *partial, int32_t *slot_rank, void *stream);
+
+/* Combine with send-side accumulation, second half: out[g] = sum of token
+ * g's used partial rows (f32 accumulation, rounded once to y_dtype). */
+int moe_combine_reduce_partials(const MoeDims *dims, const void *partial, const int32_t *slot_rank,
+                                void *out, void *stream);
 
 /* Wait for `stream`, then read the device status word written by
  * moe_dispatch_count.  Returns that status (MOE_OK or a MOE_ERR_* code), or
