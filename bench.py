@@ -419,6 +419,72 @@ def run_ours(args):
                  "note": "moe_dispatch_pack_quant on the same routing, timed alone"}
         del pq, ps
 
+    # send-side accumulation (partial rows per token and destination rank,
+    # then their sum) and the expert-parallel local path of one rank
+    next_rows = {}
+    sz = moe.buffer_sizes(dims)
+    P = sz["partial_slots"]
+    part = torch.empty(sz["partial_bytes"] // b.y.element_size(), dtype=b.y.dtype, device=dev)
+    slot_rank = torch.empty(w.NT * P, dtype=torch.int32, device=dev)
+    out2 = torch.empty_like(b.out)
+    evs2 = []
+    for i in range(nb + 3):
+        flush()
+        e = new_events(3)
+        e[0].record(stream)
+        moe.combine_partials(dims, b.y, b.pos, b.topk_w, part, slot_rank, stream)
+        e[1].record(stream)
+        moe.combine_reduce_partials(dims, part, slot_rank, out2, stream)
+        e[2].record(stream)
+        if i >= 3:
+            evs2.append(e)
+    torch.cuda.synchronize(dev)
+    used = int((slot_rank >= 0).sum().item())
+    yb = W.y_row_bytes(w)
+    t_part = statistics.mean(e[0].elapsed_time(e[1]) for e in evs2)
+    t_red = statistics.mean(e[1].elapsed_time(e[2]) for e in evs2)
+    b_part = w.NT * (yb * w.R + yb * P) + w.NT * w.R * 8
+    b_red = yb * used + w.NT * yb + w.NT * P * 4
+    next_rows["send_side_combine"] = {
+        "partials_ms": t_part, "reduce_ms": t_red, "ms": t_part + t_red,
+        "alg_bytes": b_part + b_red, "alg_gbs": (b_part + b_red) / ((t_part + t_red) / 1e3) / 1e9,
+        "partial_rows_per_token": used / w.NT,
+        "note": "moe_combine_partials + moe_combine_reduce_partials; one GPU moves more bytes "
+                "this way than the plain combine (the saving is in data sent between GPUs)"}
+    del part, slot_rank
+    d0 = 0
+    cnt_d = int(b.rank_counts[d0].item())
+    tok_d = int(((b.pos >= d0 * sz["cap_rows"]) & (b.pos < (d0 + 1) * sz["cap_rows"]))
+                .any(dim=1).sum().item())
+    evs3 = []
+    for i in range(nb + 3):
+        flush()
+        e = new_events(3)
+        e[0].record(stream)
+        moe.dispatch_pack_rank(dims, d0, inp.x, inp.x_scales, b.pos, b.packed_x, b.packed_scales,
+                               b.packed_src, stream)
+        e[1].record(stream)
+        flush()
+        e2 = new_events(2)
+        e2[0].record(stream)
+        moe.combine_rank(dims, d0, b.y, b.pos, b.topk_w, out2, stream)
+        e2[1].record(stream)
+        if i >= 3:
+            evs3.append((e[0], e[1], e2[0], e2[1]))
+    torch.cuda.synchronize(dev)
+    t_pr = statistics.mean(a.elapsed_time(c) for a, c, _, _ in evs3)
+    t_cr = statistics.mean(a.elapsed_time(c) for _, _, a, c in evs3)
+    rb = W.row_bytes(w)
+    b_pr = tok_d * rb + cnt_d * rb + cnt_d * 8
+    b_cr = cnt_d * yb + w.NT * yb + w.NT * w.R * 8
+    next_rows["ep_local_rank0"] = {
+        "pack_rank_ms": t_pr, "combine_rank_ms": t_cr, "rows": cnt_d, "tokens": tok_d,
+        "pack_rank_alg_gbs": b_pr / (t_pr / 1e3) / 1e9,
+        "combine_rank_alg_gbs": b_cr / (t_cr / 1e3) / 1e9,
+        "note": "moe_dispatch_pack_rank + moe_combine_rank for rank 0 (the all-reduce over "
+                "ranks that completes it is not part of the library)"}
+    del out2
+
     # ---- end to end through the public API with host buffers -------------
     e2e = run_e2e(args, w, dims, inp_cpu, b, dev, stream, flush, moe)
 
@@ -461,6 +527,7 @@ def run_ours(args):
                               "frac_of_8tbs_nominal": pc_gbs / 8000.0},
         "timed_segments_ms": per_timed,
         "pack_quant": quant,
+        "next_rows": next_rows,
         "kernels": kern,
         "e2e": e2e,
         "cpu_baseline": cpu,

@@ -51,8 +51,10 @@ dispatch_pack_kernel(const uint4 *__restrict__ x, const float *__restrict__ x_sc
             if (ok) packed_src[p] = (int32_t)(g * R + tid);
         }
         __syncthreads();
+        bool any = false;  // a token with no pair in the window is not read
+        for (int k = 0; k < R; ++k) any |= s_pos[k] >= 0;
         const uint4 *src = x + g * nvec;
-        for (int c0 = tid; c0 < nvec; c0 += kPackThreads * kPackVecs) {
+        for (int c0 = tid; any && c0 < nvec; c0 += kPackThreads * kPackVecs) {
             uint4 v[kPackVecs];
 #pragma unroll
             for (int u = 0; u < kPackVecs; ++u) {
