@@ -92,13 +92,15 @@ def lib() -> ctypes.CDLL:
             L.moe_combine_partials.argtypes = [D, P, P, P, P, P, P]
             L.moe_combine_reduce_partials.argtypes = [D, P, P, P, P]
             L.moe_read_status.argtypes = [P, P]
+            L.moe_take_device_error.argtypes = [P]
             L.moe_last_error.restype = ctypes.c_char_p
             L.moe_last_error.argtypes = []
             L.moe_version.restype = i32
             for fn in ("moe_buffer_sizes", "moe_route_topk", "moe_dispatch_count",
                        "moe_dispatch_pack", "moe_dispatch_pack_quant", "moe_dispatch_pack_rank",
                        "moe_combine", "moe_combine_rank", "moe_combine_partials",
-                       "moe_combine_reduce_partials", "moe_read_status"):
+                       "moe_combine_reduce_partials", "moe_read_status",
+                       "moe_take_device_error"):
                 getattr(L, fn).restype = i32
             _lib = L
     return _lib
@@ -277,6 +279,15 @@ def combine_reduce_partials(dims: MoeDims, partial, slot_rank, out, stream=None)
 def read_status(status, stream=None) -> int:
     """Wait for the stream and return the device status word of dispatch_count."""
     rc = lib().moe_read_status(_ptr(status, 4, "status", torch.int32), _stream(stream))
+    if rc == MOE_ERR_CUDA:
+        raise MoeError(rc, lib().moe_last_error().decode())
+    return rc
+
+
+def take_device_error(stream=None) -> int:
+    """Wait for the stream; return and clear the library's device error word
+    (MOE_OK, or MOE_ERR_TIMEOUT if a bounded wait in a kernel gave up)."""
+    rc = lib().moe_take_device_error(_stream(stream))
     if rc == MOE_ERR_CUDA:
         raise MoeError(rc, lib().moe_last_error().decode())
     return rc

@@ -2,6 +2,7 @@
 // one launcher per step.  See include/moe_route.h for the contract.
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "moe_internal.cuh"
@@ -91,6 +92,17 @@ int check_dims(const MoeDims *d, Derived *out, const char *what) {
     v.scales_per_row = d->x_dtype == MOE_FP8E4M3_BLK128 ? d->H / 128 : 0;
     if (out) *out = v;
     return MOE_OK;
+}
+
+// Pack kernel choice: the register-path kernel by default (the faster of
+// the two on GB300 at R = 8); the environment variable MOE_PACK_KERNEL=bulk
+// selects bulk copies through shared memory (read once per process).
+bool use_bulk_pack() {
+    static const bool bulk = [] {
+        const char *v = getenv("MOE_PACK_KERNEL");
+        return v && strcmp(v, "bulk") == 0;
+    }();
+    return bulk;
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -199,6 +211,12 @@ int moe_dispatch_pack(const MoeDims *dims, const void *x, const float *x_scales,
         return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_pack: x and packed_x must be 16-byte aligned");
     if (!aligned(pos, 4) || !aligned(packed_src, 4) || (fp8 && (!aligned(x_scales, 4) || !aligned(packed_scales, 4))))
         return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_pack: index and scale pointers must be 4-byte aligned");
+    if (use_bulk_pack() && pack_bulk_stages(v.x_row_bytes) > 0)
+        return cuda_result(launch_dispatch_pack_bulk(x, fp8 ? x_scales : nullptr, pos, v.NT, dims->R,
+                                                     v.x_row_bytes, v.scales_per_row, v.rows_total, packed_x,
+                                                     fp8 ? packed_scales : nullptr, packed_src,
+                                                     (cudaStream_t)stream),
+                           "moe_dispatch_pack");
     return cuda_result(launch_dispatch_pack(x, fp8 ? x_scales : nullptr, pos, v.NT, dims->R, v.x_row_bytes,
                                             v.scales_per_row, 0, v.rows_total, packed_x,
                                             fp8 ? packed_scales : nullptr, packed_src,
@@ -319,6 +337,14 @@ int moe_combine_reduce_partials(const MoeDims *dims, const void *partial, const 
     return cuda_result(launch_reduce_partials(partial, dims->y_dtype, slot_rank, v.NT, P, dims->H, out,
                                               (cudaStream_t)stream),
                        "moe_combine_reduce_partials");
+}
+
+int moe_take_device_error(void *stream) {
+    g_err[0] = '\0';
+    int err = 0;
+    cudaError_t e = take_device_error(&err, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_result(e, "moe_take_device_error");
+    return err;
 }
 
 int moe_read_status(const int32_t *status, void *stream) {

@@ -33,6 +33,18 @@ cudaError_t launch_dispatch_pack(const void *x, const float *x_scales, const int
                                  int64_t row_lo, int64_t row_hi, void *packed_x,
                                  float *packed_scales, int32_t *packed_src, cudaStream_t stream);
 
+// Bulk-copy pack (whole rows through shared memory); rows of more than
+// 48 KB are not supported (pack_bulk_stages returns 0).
+int pack_bulk_stages(int64_t row_bytes);
+cudaError_t launch_dispatch_pack_bulk(const void *x, const float *x_scales, const int32_t *pos,
+                                      int64_t NT, int R, int64_t row_bytes, int scales_per_row,
+                                      int64_t rows_total, void *packed_x, float *packed_scales,
+                                      int32_t *packed_src, cudaStream_t stream);
+
+// Reads and clears the library's device error word (set when a bounded
+// wait inside a kernel gives up).
+cudaError_t take_device_error(int *err, cudaStream_t stream);
+
 cudaError_t launch_dispatch_pack_quant(const void *x, const int32_t *pos, int64_t NT, int R, int H,
                                        int64_t rows_total, void *packed_q, float *packed_scales,
                                        int32_t *packed_src, cudaStream_t stream);

@@ -238,6 +238,13 @@ int moe_combine_reduce_partials(const MoeDims *dims, const void *partial, const 
  * MOE_ERR_CUDA if the wait or the copy failed. */
 int moe_read_status(const int32_t *status, void *stream);
 
+/* Wait for `stream`, then return and clear the library's device error word:
+ * MOE_OK, or MOE_ERR_TIMEOUT if a bounded wait inside one of the library's
+ * kernels gave up since the last call (that kernel's output is then
+ * incomplete).  MOE_ERR_CUDA if the wait or the copy failed.  The word is
+ * shared by every stream and thread of the process. */
+int moe_take_device_error(void *stream);
+
 /* Message for the last error returned in the calling thread ("" if none). */
 const char *moe_last_error(void);
 

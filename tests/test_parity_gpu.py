@@ -235,3 +235,38 @@ def test_cuda_graph_capture_and_replay():
     np.testing.assert_array_equal(b.topk_idx.cpu().numpy(), ref["topk_idx"])
     np.testing.assert_array_equal(b.pos.cpu().numpy(), ref["pos"])
     check_combine(w2, b.out, ref["out"], ref["mag"])
+
+
+def test_device_error_word_is_clear_after_normal_runs():
+    import combine_moe_route_topk_gb300 as moe
+    w = W.WORKLOADS["tiny"]
+    GpuRun(w, W.make_inputs(w)).combine()
+    assert moe.take_device_error() == moe.MOE_OK
+
+
+def test_bulk_pack_kernel_matches_too():
+    """The bulk-copy pack kernel (MOE_PACK_KERNEL=bulk) gives the same bytes;
+    run in a child process because the choice is read once."""
+    import os
+    import subprocess
+    import sys
+    code = (
+        "import sys; sys.path.insert(0, 'tests'); sys.path.insert(0, '.');"
+        "import numpy as np, oracle;"
+        "from combine_moe_route_topk_gb300 import workloads as W;"
+        "from gpu_path import GpuRun, compact_of_region;"
+        "ok = True\n"
+        "for name in ('tiny', 'skewed'):\n"
+        "    w = W.WORKLOADS[name]; inp = W.make_inputs(w); gr = GpuRun(w, inp)\n"
+        "    ref = oracle.run(w, inp, with_combine=False)\n"
+        "    px, ps, src = gr.packed_rows(); c = compact_of_region(gr.rows, gr.cap, ref['rank_offsets'])\n"
+        "    ok &= np.array_equal(px, ref['packed_x'][c]) and np.array_equal(src, ref['packed_src'][c])\n"
+        "    ok &= ps is None or np.array_equal(ps, ref['packed_scales'][c])\n"
+        "import combine_moe_route_topk_gb300 as moe\n"
+        "ok &= moe.take_device_error() == moe.MOE_OK\n"
+        "print('BULK_OK' if ok else 'BULK_MISMATCH')\n")
+    env = dict(os.environ, MOE_PACK_KERNEL="bulk")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True,
+                       text=True, timeout=600)
+    assert "BULK_OK" in r.stdout, r.stdout + r.stderr
