@@ -43,7 +43,7 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--e2e-steps", type=int, default=100)
-    p.add_argument("--e2e-lanes", type=int, default=2,
+    p.add_argument("--e2e-lanes", type=int, default=3,
                    help="independent buffer sets the end-to-end steps alternate between")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="CPU work for the oracle baseline (0 disables it)")

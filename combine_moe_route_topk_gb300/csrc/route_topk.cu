@@ -15,8 +15,10 @@
 //
 // Keys: z = fl32(logit + bias) is mapped to an unsigned integer whose order
 // is the float order (-0 is first turned into +0 so that the two zeros tie,
-// as they compare equal).  One round is then a single warp max reduction
-// (redux.sync) plus a ballot for the lowest lane holding the maximum.
+// as they compare equal).  Each lane sorts its keys once (bitonic network,
+// key descending, slot ascending); a round is then one warp max reduction
+// (redux.sync) over the lanes' heads, a ballot for the lowest lane holding
+// the maximum, and a register shift in that lane.
 #include <math.h>
 
 #include "moe_internal.cuh"
@@ -37,19 +39,30 @@ __device__ __forceinline__ float key_value(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Highest live key of this lane and its slot (lowest slot among equals);
-// jb = -1 when no slot is live.
-template <int J>
-__device__ __forceinline__ void local_best(const uint32_t (&key)[J], uint32_t live, uint32_t &v,
-                                           int &jb) {
-    v = 0u;
-    jb = -1;
+// Bitonic sort of a lane's (key, slot) pairs: key descending, slot
+// ascending among equal keys, so the head is always the lane's next pick.
+template <int JP>
+__device__ __forceinline__ void sort_desc(uint32_t (&k)[JP], int (&sl)[JP]) {
 #pragma unroll
-    for (int j = 0; j < J; ++j) {
-        if ((live >> j) & 1u) {
-            if (jb < 0 || key[j] > v) {
-                v = key[j];
-                jb = j;
+    for (int size = 2; size <= JP; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+            for (int i = 0; i < JP; ++i) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    // descending runs where (i & size) == 0, ascending otherwise
+                    const bool desc = (i & size) == 0;
+                    const bool i_first = k[i] > k[j] || (k[i] == k[j] && sl[i] < sl[j]);
+                    if (desc != i_first) {
+                        const uint32_t tk = k[i];
+                        k[i] = k[j];
+                        k[j] = tk;
+                        const int ts = sl[i];
+                        sl[i] = sl[j];
+                        sl[j] = ts;
+                    }
+                }
             }
         }
     }
@@ -89,31 +102,43 @@ route_topk_kernel(const float *__restrict__ logits, const float *__restrict__ bi
         for (int j = 0; j < J; ++j)
             if (e0 + j < E) z[j] = __ldg(row + e0 + j);
     }
+    // JP >= J slots (a power of two for the sorting network); padding
+    // slots carry key 0 and sort last
+    constexpr int JP = (J <= 1) ? 1 : (J <= 2) ? 2 : (J <= 4) ? 4 : (J <= 8) ? 8 : (J <= 16) ? 16 : 32;
     uint32_t valid = 0;
-    uint32_t key[J];
+    uint32_t key[JP];
+    int slot[JP];
 #pragma unroll
-    for (int j = 0; j < J; ++j) {
+    for (int j = 0; j < JP; ++j) {
         key[j] = 0u;
-        if (e0 + j < E) {
+        slot[j] = j;
+        if (j < J && e0 + j < E) {
             valid |= 1u << j;
             if (bias != nullptr) z[j] = __fadd_rn(z[j], __ldg(bias + e0 + j));
             key[j] = order_key(z[j]);
         }
     }
+    int left = __popc(valid);  // live keys of this lane
+    uint32_t sk[JP];
+    int ss[JP];
+#pragma unroll
+    for (int j = 0; j < JP; ++j) {
+        sk[j] = key[j];
+        ss[j] = slot[j];
+    }
+    sort_desc<JP>(sk, ss);
 
-    // R rounds of warp arg-max; only the winning lane rescans its slots.
-    uint32_t live = valid;
-    uint32_t v;
-    int jb;
-    local_best<J>(key, live, v, jb);
+    // R rounds of warp arg-max over the lanes' heads; the winning lane pops
+    // its head (a register shift, no rescan).
     float zmax = 0.f;
     int my_e = 0;
     float my_z = 0.f;
     for (int k = 0; k < R; ++k) {
+        const uint32_t v = (left > 0) ? sk[0] : 0u;
         const uint32_t kmax = __reduce_max_sync(kFull, v);
-        const unsigned ball = __ballot_sync(kFull, jb >= 0 && v == kmax);
-        const int wl = __ffs(ball) - 1;  // some lane always has a live slot (R <= E)
-        const int wj = __shfl_sync(kFull, jb, wl);
+        const unsigned ball = __ballot_sync(kFull, left > 0 && v == kmax);
+        const int wl = __ffs(ball) - 1;  // some lane always has a live key (R <= E)
+        const int wj = __shfl_sync(kFull, ss[0], wl);
         const float wz = key_value(kmax);
         if (k == 0) zmax = wz;
         if (lane == k) {
@@ -121,8 +146,12 @@ route_topk_kernel(const float *__restrict__ logits, const float *__restrict__ bi
             my_z = wz;
         }
         if (lane == wl) {
-            live &= ~(1u << wj);
-            local_best<J>(key, live, v, jb);
+#pragma unroll
+            for (int j = 0; j + 1 < JP; ++j) {
+                sk[j] = sk[j + 1];
+                ss[j] = ss[j + 1];
+            }
+            --left;
         }
     }
 
