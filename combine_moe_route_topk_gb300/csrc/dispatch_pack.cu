@@ -41,6 +41,21 @@ dispatch_pack_kernel(const uint4 *__restrict__ x, const float *__restrict__ x_sc
                      float *__restrict__ packed_scales, int32_t *__restrict__ packed_src) {
     __shared__ int s_pos[32];
     const int tid = threadIdx.x;
+    // The first token's row is loaded before waiting for the previous kernel:
+    // x is not produced by the count kernel (only pos is), and every kernel
+    // of this library lets its dependents start only after its own inputs
+    // are final, so the row is complete here.  This overlaps the row load
+    // with the tail of the count kernel.
+    const int64_t g_first = blockIdx.x;
+    const bool preload = g_first < NT && nvec <= kPackThreads * kPackVecs;
+    uint4 pre[kPackVecs];
+    if (preload) {
+#pragma unroll
+        for (int u = 0; u < kPackVecs; ++u) {
+            const int c = tid + u * kPackThreads;
+            if (c < nvec) pre[u] = ld_stream(x + g_first * nvec + c);
+        }
+    }
     grid_dependency_wait();  // pos comes from the count kernel
     grid_launch_dependents();
     for (int64_t g = blockIdx.x; g < NT; g += gridDim.x) {
@@ -56,10 +71,15 @@ dispatch_pack_kernel(const uint4 *__restrict__ x, const float *__restrict__ x_sc
         const uint4 *src = x + g * nvec;
         for (int c0 = tid; any && c0 < nvec; c0 += kPackThreads * kPackVecs) {
             uint4 v[kPackVecs];
+            if (preload && g == g_first) {
 #pragma unroll
-            for (int u = 0; u < kPackVecs; ++u) {
-                const int c = c0 + u * kPackThreads;
-                if (c < nvec) v[u] = ld_stream(src + c);
+                for (int u = 0; u < kPackVecs; ++u) v[u] = pre[u];
+            } else {
+#pragma unroll
+                for (int u = 0; u < kPackVecs; ++u) {
+                    const int c = c0 + u * kPackThreads;
+                    if (c < nvec) v[u] = ld_stream(src + c);
+                }
             }
             for (int k = 0; k < R; ++k) {
                 const int p = s_pos[k];
