@@ -419,6 +419,39 @@ def run_ours(args):
                  "note": "moe_dispatch_pack_quant on the same routing, timed alone"}
         del pq, ps
 
+    # decode-fused dispatch (route + count + pack in one launch) on the same
+    # inputs, when the batch is a decode batch it supports
+    fused = None
+    try:
+        ws = torch.empty(moe.buffer_sizes(dims)["fused_workspace_bytes"], dtype=torch.uint8,
+                         device=dev)
+
+        def fused_call():
+            moe.dispatch_fused(dims, inp.logits, inp.bias, w.score_fn, w.renormalize, inp.x,
+                               inp.x_scales, b.topk_idx, b.topk_w, b.expert_counts,
+                               b.expert_offsets, b.rank_counts, b.rank_offsets, b.send_counts,
+                               b.pos, b.status, b.packed_x, b.packed_scales, b.packed_src, ws,
+                               stream)
+        fe = []
+        for i in range(nb + 3):
+            flush()
+            e0, e1 = new_events(2)
+            e0.record(stream)
+            fused_call()
+            e1.record(stream)
+            if i >= 3:
+                fe.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        if moe.read_status(b.status, stream) != moe.MOE_OK:
+            raise RuntimeError("fused dispatch status")
+        fm = statistics.mean(a.elapsed_time(c) for a, c in fe)
+        fused = {"ms": fm, "vs_separate_dispatch_ms": per_timed["dispatch (route+count+pack)"],
+                 "step_ms_if_used": fm + per_timed["combine"],
+                 "note": "moe_dispatch_fused (one cooperative launch) on the same batch"}
+        del ws
+    except moe.MoeError as ex:
+        fused = {"unsupported": str(ex)}
+
     # send-side accumulation (partial rows per token and destination rank,
     # then their sum) and the expert-parallel local path of one rank
     next_rows = {}
@@ -527,6 +560,7 @@ def run_ours(args):
                               "frac_of_8tbs_nominal": pc_gbs / 8000.0},
         "timed_segments_ms": per_timed,
         "pack_quant": quant,
+        "fused_dispatch": fused,
         "next_rows": next_rows,
         "kernels": kern,
         "e2e": e2e,

@@ -154,6 +154,7 @@ int moe_buffer_sizes(const MoeDims *dims, MoeSizes *out) {
     out->partial_slots = dims->R < N ? dims->R : N;
     out->partial_bytes = v.NT * out->partial_slots * v.y_row_bytes;
     out->slot_rank_bytes = v.NT * out->partial_slots * 4;
+    out->fused_workspace_bytes = fused_workspace_bytes(dims->E);
     (void)H;
     return MOE_OK;
 }
@@ -337,6 +338,45 @@ int moe_combine_reduce_partials(const MoeDims *dims, const void *partial, const 
     return cuda_result(launch_reduce_partials(partial, dims->y_dtype, slot_rank, v.NT, P, dims->H, out,
                                               (cudaStream_t)stream),
                        "moe_combine_reduce_partials");
+}
+
+int moe_dispatch_fused(const MoeDims *dims, const float *logits, const float *bias, int score_fn,
+                       int renormalize, const void *x, const float *x_scales, int32_t *topk_idx,
+                       float *topk_w, int32_t *expert_counts, int32_t *expert_offsets,
+                       int32_t *rank_counts, int32_t *rank_offsets, int32_t *send_counts, int32_t *pos,
+                       int32_t *status, void *packed_x, float *packed_scales, int32_t *packed_src,
+                       void *workspace, void *stream) {
+    Derived v;
+    int rc = check_dims(dims, &v, "moe_dispatch_fused");
+    if (rc != MOE_OK) return rc;
+    if (score_fn != MOE_SOFTMAX && score_fn != MOE_SIGMOID)
+        return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_fused: unknown score_fn %d", score_fn);
+    const char *why = fused_unsupported(dims->N, dims->T, dims->E, dims->R);
+    if (why[0] != '\0')
+        return set_error(MOE_ERR_UNSUPPORTED, "moe_dispatch_fused: %s; use the separate calls", why);
+    const bool fp8 = dims->x_dtype == MOE_FP8E4M3_BLK128;
+    if (!expert_counts || !expert_offsets || !rank_counts || !rank_offsets || !send_counts || !status ||
+        !workspace)
+        return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_fused: a required pointer is NULL");
+    if (v.NT > 0 && (!logits || !x || !topk_idx || !topk_w || !pos || !packed_x || !packed_src ||
+                     (fp8 && (!x_scales || !packed_scales))))
+        return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_fused: a required pointer is NULL");
+    if ((x && !aligned(x, 16)) || (packed_x && !aligned(packed_x, 16)) || !aligned(workspace, 16))
+        return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_fused: x, packed_x and workspace must be 16-byte aligned");
+    const void *ptrs4[] = {logits, bias, topk_idx, topk_w, expert_counts, expert_offsets, rank_counts,
+                           rank_offsets, send_counts, pos, status, packed_src, x_scales, packed_scales};
+    for (const void *p : ptrs4)
+        if (p && !aligned(p, 4))
+            return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_fused: pointers must be 4-byte aligned");
+    cudaError_t e = launch_dispatch_fused(logits, bias, score_fn, renormalize ? 1 : 0, x, fp8 ? x_scales : nullptr,
+                                          dims->N, dims->T, dims->E, dims->R, v.x_row_bytes, v.scales_per_row,
+                                          v.cap, topk_idx, topk_w, expert_counts, expert_offsets, rank_counts,
+                                          rank_offsets, send_counts, pos, status, packed_x,
+                                          fp8 ? packed_scales : nullptr, packed_src, workspace,
+                                          (cudaStream_t)stream);
+    if (e == cudaErrorNotSupported || e == cudaErrorCooperativeLaunchTooLarge)
+        return set_error(MOE_ERR_UNSUPPORTED, "moe_dispatch_fused: the device cannot hold enough co-resident blocks");
+    return cuda_result(e, "moe_dispatch_fused");
 }
 
 int moe_take_device_error(void *stream) {

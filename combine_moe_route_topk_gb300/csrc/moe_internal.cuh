@@ -45,6 +45,17 @@ cudaError_t launch_dispatch_pack_bulk(const void *x, const float *x_scales, cons
 // wait inside a kernel gives up).
 cudaError_t take_device_error(int *err, cudaStream_t stream);
 
+// Decode-fused route + count + pack (one cooperative launch).
+int64_t fused_workspace_bytes(int E);
+const char *fused_unsupported(int N, int T, int E, int R);  // "" when supported
+cudaError_t launch_dispatch_fused(const float *logits, const float *bias, int score_fn, int renormalize,
+                                  const void *x, const float *x_scales, int N, int T, int E, int R,
+                                  int64_t row_bytes, int spr, int64_t cap, int32_t *topk_idx,
+                                  float *topk_w, int32_t *expert_counts, int32_t *expert_offsets,
+                                  int32_t *rank_counts, int32_t *rank_offsets, int32_t *send_counts,
+                                  int32_t *pos, int32_t *status, void *packed_x, float *packed_scales,
+                                  int32_t *packed_src, void *workspace, cudaStream_t stream);
+
 cudaError_t launch_dispatch_pack_quant(const void *x, const int32_t *pos, int64_t NT, int R, int H,
                                        int64_t rows_total, void *packed_q, float *packed_scales,
                                        int32_t *packed_src, cudaStream_t stream);

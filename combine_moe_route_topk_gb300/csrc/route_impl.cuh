@@ -1,0 +1,161 @@
+// Per-token body of the route top-k step, shared by the route kernel and
+// the decode-fused dispatch kernel.  See route_topk.cu for the method and
+// its sources.
+#pragma once
+
+#include <math.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace route_impl {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ uint32_t order_key(float v) {
+    const uint32_t u = __float_as_uint(__fadd_rn(v, 0.0f));  // -0 -> +0
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Bitonic sort of a lane's (key, slot) pairs: key descending, slot
+// ascending among equal keys, so the head is always the lane's next pick.
+template <int JP>
+__device__ __forceinline__ void sort_desc(uint32_t (&k)[JP], int (&sl)[JP]) {
+#pragma unroll
+    for (int size = 2; size <= JP; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+            for (int i = 0; i < JP; ++i) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    // descending runs where (i & size) == 0, ascending otherwise
+                    const bool desc = (i & size) == 0;
+                    const bool i_first = k[i] > k[j] || (k[i] == k[j] && sl[i] < sl[j]);
+                    if (desc != i_first) {
+                        const uint32_t tk = k[i];
+                        k[i] = k[j];
+                        k[j] = tk;
+                        const int ts = sl[i];
+                        sl[i] = sl[j];
+                        sl[j] = ts;
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Route token g with the calling warp (all 32 lanes).
+template <int J, bool kVec4>
+__device__ __forceinline__ void route_token(const float *__restrict__ logits,
+                                            const float *__restrict__ bias, int64_t g, int E, int R,
+                                            int score_fn, int renormalize,
+                                            int32_t *__restrict__ topk_idx,
+                                            float *__restrict__ topk_w, int lane) {
+    const float *row = logits + g * E;
+    const int e0 = lane * J;
+    float z[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) z[j] = 0.f;
+    if (kVec4) {
+        // E % 4 == 0 and J % 4 == 0: e0 + j is a multiple of 4, so the
+        // 16-byte load is aligned and stays inside the row.
+#pragma unroll
+        for (int j = 0; j < J; j += 4) {
+            if (e0 + j < E) {
+                const float4 v = __ldg(reinterpret_cast<const float4 *>(row + e0 + j));
+                z[j] = v.x;
+                z[j + 1] = v.y;
+                z[j + 2] = v.z;
+                z[j + 3] = v.w;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < J; ++j)
+            if (e0 + j < E) z[j] = __ldg(row + e0 + j);
+    }
+    // JP >= J slots (a power of two for the sorting network); padding
+    // slots carry key 0 and sort last
+    constexpr int JP = (J <= 1) ? 1 : (J <= 2) ? 2 : (J <= 4) ? 4 : (J <= 8) ? 8 : (J <= 16) ? 16 : 32;
+    uint32_t valid = 0;
+    uint32_t key[JP];
+    int slot[JP];
+#pragma unroll
+    for (int j = 0; j < JP; ++j) {
+        key[j] = 0u;
+        slot[j] = j;
+        if (j < J && e0 + j < E) {
+            valid |= 1u << j;
+            if (bias != nullptr) z[j] = __fadd_rn(z[j], __ldg(bias + e0 + j));
+            key[j] = order_key(z[j]);
+        }
+    }
+    int left = __popc(valid);  // live keys of this lane
+    uint32_t sk[JP];
+    int ss[JP];
+#pragma unroll
+    for (int j = 0; j < JP; ++j) {
+        sk[j] = key[j];
+        ss[j] = slot[j];
+    }
+    sort_desc<JP>(sk, ss);
+
+    // R rounds of warp arg-max over the lanes' heads; the winning lane pops
+    // its head (a register shift, no rescan).
+    float zmax = 0.f;
+    int my_e = 0;
+    float my_z = 0.f;
+    for (int k = 0; k < R; ++k) {
+        const uint32_t v = (left > 0) ? sk[0] : 0u;
+        const uint32_t kmax = __reduce_max_sync(kFull, v);
+        const unsigned ball = __ballot_sync(kFull, left > 0 && v == kmax);
+        const int wl = __ffs(ball) - 1;  // some lane always has a live key (R <= E)
+        const int wj = __shfl_sync(kFull, ss[0], wl);
+        const float wz = key_value(kmax);
+        if (k == 0) zmax = wz;
+        if (lane == k) {
+            my_e = wl * J + wj;
+            my_z = wz;
+        }
+        if (lane == wl) {
+#pragma unroll
+            for (int j = 0; j + 1 < JP; ++j) {
+                sk[j] = sk[j + 1];
+                ss[j] = ss[j + 1];
+            }
+            --left;
+        }
+    }
+
+    float p = 0.f;
+    if (score_fn == MOE_SOFTMAX) {
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < J; ++j)
+            if ((valid >> j) & 1u) s += expf(key_value(key[j]) - zmax);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
+        if (lane < R) p = expf(my_z - zmax) / s;
+    } else {
+        if (lane < R) p = 1.0f / (1.0f + expf(-my_z));
+    }
+    if (renormalize) {
+        float t = p;  // lanes >= R hold 0
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(kFull, t, off);
+        p = p / t;
+    }
+    if (lane < R) {
+        topk_idx[g * R + lane] = my_e;
+        topk_w[g * R + lane] = p;
+    }
+}
+
+}  // namespace route_impl
+}  // namespace moe

@@ -92,6 +92,7 @@ typedef struct MoeSizes {
     int64_t partial_slots;       /* P = min(R, N): partial rows per token */
     int64_t partial_bytes;       /* [N*T][P][H] of y_dtype (moe_combine_partials) */
     int64_t slot_rank_bytes;     /* i32 [N*T][P] */
+    int64_t fused_workspace_bytes; /* workspace of moe_dispatch_fused */
 } MoeSizes;
 
 /* Fill *out with the buffer sizes for dims (host only, no CUDA call).
@@ -165,6 +166,25 @@ int moe_dispatch_count(const MoeDims *dims, const int32_t *topk_idx, int32_t *ex
 int moe_dispatch_pack(const MoeDims *dims, const void *x, const float *x_scales,
                       const int32_t *pos, void *packed_x, float *packed_scales,
                       int32_t *packed_src, void *stream);
+
+/* Decode-fused dispatch: moe_route_topk, moe_dispatch_count and
+ * moe_dispatch_pack in one launch, with the same arguments and identical
+ * outputs.  Source: "Hosting Qwen on Blackwell", section "Expert parallel"
+ * (for decode the whole dispatch kernel is fused into one).
+ *   workspace  device scratch of MoeSizes.fused_workspace_bytes bytes,
+ *              16-byte aligned, owned by the caller; calls that may run at
+ *              the same time need separate workspaces.
+ * Decode batches only: N*T <= 4096, T % 32 == 0, R <= 8, E <= 512 (else
+ * MOE_ERR_UNSUPPORTED before anything is enqueued: use the three calls).
+ * The kernel is a cooperative launch (all its blocks are resident at once)
+ * whose phases meet at grid-wide barriers; each barrier wait is bounded,
+ * and one that gives up leaves MOE_ERR_TIMEOUT in *status. */
+int moe_dispatch_fused(const MoeDims *dims, const float *logits, const float *bias, int score_fn,
+                       int renormalize, const void *x, const float *x_scales, int32_t *topk_idx,
+                       float *topk_w, int32_t *expert_counts, int32_t *expert_offsets,
+                       int32_t *rank_counts, int32_t *rank_offsets, int32_t *send_counts, int32_t *pos,
+                       int32_t *status, void *packed_x, float *packed_scales, int32_t *packed_src,
+                       void *workspace, void *stream);
 
 /* Dispatch pack with fp8 block quantisation fused in.  Source: "Lower
  * latency and higher throughput with multi-node DeepSeek deployment",

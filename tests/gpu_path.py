@@ -54,7 +54,8 @@ def expert_op_gpu(w: W.Workload, bufs: moe.Buffers, rows: torch.Tensor) -> None:
 class GpuRun:
     """Route -> count -> pack -> (expert op) -> combine on the current GPU."""
 
-    def __init__(self, w: W.Workload, inp: W.Inputs, topk_idx_override: np.ndarray | None = None):
+    def __init__(self, w: W.Workload, inp: W.Inputs, topk_idx_override: np.ndarray | None = None,
+                 fused: bool = False):
         self.w = w
         self.dims = moe.dims_of(w)
         dev = torch.device("cuda", torch.cuda.current_device())
@@ -62,14 +63,22 @@ class GpuRun:
                             for t in (inp.logits, inp.bias, inp.x, inp.x_scales)))
         self.bufs = moe.Buffers(self.dims, device=dev)
         b = self.bufs
-        moe.route_topk(self.dims, self.d.logits, self.d.bias, w.score_fn, w.renormalize,
-                       b.topk_idx, b.topk_w)
-        if topk_idx_override is not None:
-            b.topk_idx.copy_(torch.from_numpy(np.ascontiguousarray(topk_idx_override)))
-        moe.dispatch_count(self.dims, b.topk_idx, b.expert_counts, b.expert_offsets,
-                           b.rank_counts, b.rank_offsets, b.send_counts, b.pos, b.status)
-        moe.dispatch_pack(self.dims, self.d.x, self.d.x_scales, b.pos, b.packed_x,
-                          b.packed_scales, b.packed_src)
+        if fused:
+            assert topk_idx_override is None
+            ws = torch.empty(b.sizes["fused_workspace_bytes"], dtype=torch.uint8, device=dev)
+            moe.dispatch_fused(self.dims, self.d.logits, self.d.bias, w.score_fn, w.renormalize,
+                               self.d.x, self.d.x_scales, b.topk_idx, b.topk_w, b.expert_counts,
+                               b.expert_offsets, b.rank_counts, b.rank_offsets, b.send_counts,
+                               b.pos, b.status, b.packed_x, b.packed_scales, b.packed_src, ws)
+        else:
+            moe.route_topk(self.dims, self.d.logits, self.d.bias, w.score_fn, w.renormalize,
+                           b.topk_idx, b.topk_w)
+            if topk_idx_override is not None:
+                b.topk_idx.copy_(torch.from_numpy(np.ascontiguousarray(topk_idx_override)))
+            moe.dispatch_count(self.dims, b.topk_idx, b.expert_counts, b.expert_offsets,
+                               b.rank_counts, b.rank_offsets, b.send_counts, b.pos, b.status)
+            moe.dispatch_pack(self.dims, self.d.x, self.d.x_scales, b.pos, b.packed_x,
+                              b.packed_scales, b.packed_src)
         self.status = moe.read_status(b.status)
         self.cap = b.sizes["cap_rows"]
         self.host = {k: getattr(b, k).cpu().numpy() for k in

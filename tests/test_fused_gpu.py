@@ -1,0 +1,66 @@
+"""Parity of the decode-fused dispatch (route + count + pack in one
+cooperative launch) with the oracle; same bar as the separate calls:
+indices, counts, positions and packed rows bit-exact, weights within 2e-6,
+combine within the combine tolerance."""
+import numpy as np
+import pytest
+import torch
+
+import combine_moe_route_topk_gb300 as moe
+import oracle
+from combine_moe_route_topk_gb300 import workloads as W
+from gpu_path import GpuRun
+from test_parity_gpu import _compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from combine_moe_route_topk_gb300 import _build
+    _build.build()
+
+
+@pytest.mark.parametrize("name", ["tiny", "dsv3_decode", "kimi_k2_decode"])
+def test_fused_full_size_decode(name):
+    w = W.WORKLOADS[name]
+    gr, _, _ = _compare(w, W.make_inputs(w), fused=True)
+    assert gr.status == oracle.OK
+
+
+CASES = {
+    # ties, sigmoid without renormalisation, a bias
+    "ties_sigmoid": W.Workload("ties_sigmoid", N=8, T=32, E=64, R=6, H=256, score_fn=W.SIGMOID,
+                               bias="normal", seed=61),
+    # one expert per rank, f32 rows, ragged last count block (N*T = 700 is not a multiple of 256)
+    "f32_ragged": W.Workload("f32_ragged", N=7, T=96, E=14, R=2, H=72, x_dtype=W.F32,
+                             y_dtype=W.F32, renormalize=True, seed=62),
+    # fp8 rows with block scales
+    "fp8": W.Workload("fp8", N=8, T=64, E=64, R=4, H=512, x_dtype=W.FP8E4M3_BLK128,
+                      expert_op=W.EXPERT_DEQUANT, seed=63),
+    # more experts per lane (E = 512)
+    "e512": W.Workload("e512", N=16, T=64, E=512, R=8, H=128, renormalize=True, seed=64),
+    # capacity overflow reported through the status word
+    "capacity": W.Workload("capacity", N=4, T=64, E=16, R=2, H=128, cap_rows=100, seed=65),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_fused_cases(name):
+    w = CASES[name]
+    inp = W.make_inputs(w, tie_every=3 if name == "ties_sigmoid" else 0)
+    gr, _, _ = _compare(w, inp, fused=True)
+    assert gr.status == (oracle.ERR_CAPACITY if name == "capacity" else oracle.OK)
+
+
+def test_fused_equals_separate_calls_bytewise():
+    w = W.WORKLOADS["dsv3_decode"]
+    inp = W.make_inputs(w)
+    a = GpuRun(w, inp, fused=True)
+    b = GpuRun(w, inp)
+    for k in a.host:
+        np.testing.assert_array_equal(a.host[k], b.host[k], err_msg=k)
+    pa, _, sa = a.packed_rows()
+    pb, _, sb = b.packed_rows()
+    np.testing.assert_array_equal(pa, pb)
+    np.testing.assert_array_equal(sa, sb)

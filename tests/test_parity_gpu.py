@@ -41,8 +41,8 @@ def _oracle_route_count(w, inp):
     return idx, tw, cnt, st
 
 
-def _compare(w, inp, topk_idx_override=None, combine_tokens=None):
-    gr = GpuRun(w, inp, topk_idx_override=topk_idx_override)
+def _compare(w, inp, topk_idx_override=None, combine_tokens=None, fused=False):
+    gr = GpuRun(w, inp, topk_idx_override=topk_idx_override, fused=fused)
     h = gr.host
     idx, tw, cnt, st = _oracle_route_count(w, inp)
     # route (the count input is replaced afterwards when a test overrides it)
