@@ -90,6 +90,8 @@ def lib() -> ctypes.CDLL:
             L.moe_dispatch_pack_rank.argtypes = [D, i32, P, P, P, P, P, P, P]
             L.moe_dispatch_fused.argtypes = [D, P, P, i32, i32, P, P, P, P, P, P, P, P, P, P, P,
                                              P, P, P, P, P]
+            L.moe_dispatch_fused_static.argtypes = [D, P, P, i32, i32, P, P, P, P, P, P, P, P, P,
+                                                    P, P, P, P, P, P]
             L.moe_combine_rank.argtypes = [D, i32, P, P, P, P, P]
             L.moe_combine_partials.argtypes = [D, P, P, P, P, P, P]
             L.moe_combine_reduce_partials.argtypes = [D, P, P, P, P]
@@ -100,7 +102,7 @@ def lib() -> ctypes.CDLL:
             L.moe_version.restype = i32
             for fn in ("moe_buffer_sizes", "moe_route_topk", "moe_dispatch_count",
                        "moe_dispatch_pack", "moe_dispatch_pack_quant", "moe_dispatch_pack_rank",
-                       "moe_dispatch_fused",
+                       "moe_dispatch_fused", "moe_dispatch_fused_static",
                        "moe_combine", "moe_combine_rank", "moe_combine_partials",
                        "moe_combine_reduce_partials", "moe_read_status",
                        "moe_take_device_error"):
@@ -226,6 +228,34 @@ def dispatch_fused(dims: MoeDims, logits, bias, score_fn, renormalize, x, x_scal
         _ptr(packed_scales, s["packed_scales_bytes"], "packed_scales", f32, optional=not fp8),
         _ptr(packed_src, s["packed_src_bytes"], "packed_src", i32),
         _ptr(workspace, s["fused_workspace_bytes"], "workspace"), _stream(stream)))
+
+
+def dispatch_fused_static(dims: MoeDims, logits, bias, score_fn, renormalize, x, x_scales,
+                          topk_idx, topk_w, expert_counts, expert_offsets, rank_counts,
+                          rank_offsets, send_counts, pos, status, packed_x, packed_scales,
+                          packed_src, stream=None):
+    """moe_dispatch_fused with the library's own static scratch: nothing is
+    allocated by the call (for callers that cannot allocate device memory
+    when they dispatch).  Calls that overlap on the GPU race on the scratch."""
+    s = buffer_sizes(dims)
+    i32, f32 = torch.int32, torch.float32
+    fp8 = dims.x_dtype == MOE_FP8E4M3_BLK128
+    _check(lib().moe_dispatch_fused_static(
+        ctypes.byref(dims), _ptr(logits, s["logits_bytes"], "logits", f32),
+        _ptr(bias, dims.E * 4, "bias", f32, optional=True), int(score_fn), int(bool(renormalize)),
+        _ptr(x, s["x_bytes"], "x", _TORCH_DTYPE[dims.x_dtype]),
+        _ptr(x_scales, s["x_scales_bytes"], "x_scales", f32, optional=not fp8),
+        _ptr(topk_idx, s["topk_idx_bytes"], "topk_idx", i32),
+        _ptr(topk_w, s["topk_w_bytes"], "topk_w", f32),
+        _ptr(expert_counts, s["expert_counts_bytes"], "expert_counts", i32),
+        _ptr(expert_offsets, s["expert_offsets_bytes"], "expert_offsets", i32),
+        _ptr(rank_counts, s["rank_counts_bytes"], "rank_counts", i32),
+        _ptr(rank_offsets, s["rank_offsets_bytes"], "rank_offsets", i32),
+        _ptr(send_counts, s["send_counts_bytes"], "send_counts", i32),
+        _ptr(pos, s["pos_bytes"], "pos", i32), _ptr(status, 4, "status", i32),
+        _ptr(packed_x, s["packed_x_bytes"], "packed_x", _TORCH_DTYPE[dims.x_dtype]),
+        _ptr(packed_scales, s["packed_scales_bytes"], "packed_scales", f32, optional=not fp8),
+        _ptr(packed_src, s["packed_src_bytes"], "packed_src", i32), _stream(stream)))
 
 
 def fp8_dims(dims: MoeDims) -> MoeDims:

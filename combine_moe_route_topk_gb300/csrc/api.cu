@@ -379,6 +379,31 @@ int moe_dispatch_fused(const MoeDims *dims, const float *logits, const float *bi
     return cuda_result(e, "moe_dispatch_fused");
 }
 
+int moe_dispatch_fused_static(const MoeDims *dims, const float *logits, const float *bias, int score_fn,
+                              int renormalize, const void *x, const float *x_scales, int32_t *topk_idx,
+                              float *topk_w, int32_t *expert_counts, int32_t *expert_offsets,
+                              int32_t *rank_counts, int32_t *rank_offsets, int32_t *send_counts,
+                              int32_t *pos, int32_t *status, void *packed_x, float *packed_scales,
+                              int32_t *packed_src, void *stream) {
+    Derived v;
+    int rc = check_dims(dims, &v, "moe_dispatch_fused_static");
+    if (rc != MOE_OK) return rc;
+    const char *why = fused_unsupported(dims->N, dims->T, dims->E, dims->R);
+    if (why[0] != '\0')
+        return set_error(MOE_ERR_UNSUPPORTED, "moe_dispatch_fused_static: %s; use the separate calls", why);
+    const int64_t need = fused_workspace_bytes(dims->E);
+    if (need > fused_static_scratch_bytes())
+        return set_error(MOE_ERR_UNSUPPORTED,
+                         "moe_dispatch_fused_static: E=%d needs %lld bytes of scratch; the library's static "
+                         "array holds %lld", dims->E, (long long)need, (long long)fused_static_scratch_bytes());
+    void *scratch = nullptr;
+    cudaError_t e = fused_static_scratch(&scratch);
+    if (e != cudaSuccess) return cuda_result(e, "moe_dispatch_fused_static: scratch address");
+    return moe_dispatch_fused(dims, logits, bias, score_fn, renormalize, x, x_scales, topk_idx, topk_w,
+                              expert_counts, expert_offsets, rank_counts, rank_offsets, send_counts, pos,
+                              status, packed_x, packed_scales, packed_src, scratch, stream);
+}
+
 int moe_take_device_error(void *stream) {
     g_err[0] = '\0';
     int err = 0;

@@ -26,6 +26,8 @@
 // Scope: decode batches (N*T <= 4096), T % 32 == 0, R <= 8, E <= 512; the
 // host rejects anything else with MOE_ERR_UNSUPPORTED (use the three
 // separate calls).
+#include <mutex>
+
 #include "moe_internal.cuh"
 #include "route_impl.cuh"
 
@@ -539,6 +541,51 @@ cudaError_t launch_dispatch_fused(const float *logits, const float *bias, int sc
     if (need <= 8) return launch_fused_j<8>(P, stream);
     if (need <= 12) return launch_fused_j<12>(P, stream);
     return launch_fused_j<16>(P, stream);
+}
+
+}  // namespace moe
+
+// ---- allocation-free variant -------------------------------------------------
+//
+// Some callers cannot allocate device memory at the point where they
+// dispatch: a plug-in running inside another framework's execution loop has
+// no allocator of its own, and serving code whose memory is fixed at
+// start-up must not call cudaMalloc on its hot path (it synchronises the
+// device and can fail under memory pressure).  For them the fused dispatch
+// can use scratch that lives in the library itself: a fixed array in device
+// memory, reserved on every GPU that loads the library for as long as the
+// process runs.  Its size covers the workspace of every batch the fused
+// kernel accepts (E <= 512 needs at most 164,288 bytes).
+namespace moe {
+
+constexpr int64_t kStaticScratchBytes = 192 * 1024;
+static __device__ __align__(256) unsigned char g_fused_static_scratch[kStaticScratchBytes];
+
+namespace {
+constexpr int kMaxScratchDevices = 64;
+std::mutex g_scratch_mutex;
+void *g_scratch_addr[kMaxScratchDevices] = {};
+}  // namespace
+
+int64_t fused_static_scratch_bytes() { return kStaticScratchBytes; }
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name only stands in for it, so the address is looked up once
+// per device (with that device current) and cached.
+cudaError_t fused_static_scratch(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxScratchDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_addr[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_fused_static_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return cudaSuccess;
 }
 
 }  // namespace moe

@@ -56,6 +56,11 @@ cudaError_t launch_dispatch_fused(const float *logits, const float *bias, int sc
                                   int32_t *pos, int32_t *status, void *packed_x, float *packed_scales,
                                   int32_t *packed_src, void *workspace, cudaStream_t stream);
 
+// Scratch for the allocation-free fused dispatch: a fixed device array of
+// the library (size in bytes; address on the current device).
+int64_t fused_static_scratch_bytes();
+cudaError_t fused_static_scratch(void **out);
+
 cudaError_t launch_dispatch_pack_quant(const void *x, const int32_t *pos, int64_t NT, int R, int H,
                                        int64_t rows_total, void *packed_q, float *packed_scales,
                                        int32_t *packed_src, cudaStream_t stream);

@@ -186,6 +186,32 @@ int moe_dispatch_fused(const MoeDims *dims, const float *logits, const float *bi
                        int32_t *status, void *packed_x, float *packed_scales, int32_t *packed_src,
                        void *workspace, void *stream);
 
+/* moe_dispatch_fused without a workspace argument: for callers that cannot
+ * allocate device memory when they dispatch (a plug-in inside another
+ * framework's execution loop that has no allocator of its own, or serving
+ * code whose memory is fixed at start-up and must not call cudaMalloc on
+ * its hot path, where it would synchronise the device and could fail under
+ * memory pressure).  The pages have no counterpart: this is a deployment
+ * convenience of this library.
+ *   Scratch: a fixed array of 192 KiB in the library's device memory,
+ *   reserved on every GPU that loads the library until the process exits
+ *   (enough for every batch moe_dispatch_fused accepts: E <= 512 needs at
+ *   most 164,288 bytes; larger needs are rejected with MOE_ERR_UNSUPPORTED).
+ *   The first call on a device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   The call itself allocates nothing.
+ *   Every call shares the one array, which keeps the last call's contents;
+ *   each call clears the words that must start at zero.  Calls that overlap
+ *   on the GPU (other streams, other host threads) race on the array and
+ *   must be ordered by the caller.
+ * Other arguments, outputs and limits as moe_dispatch_fused. */
+int moe_dispatch_fused_static(const MoeDims *dims, const float *logits, const float *bias, int score_fn,
+                              int renormalize, const void *x, const float *x_scales, int32_t *topk_idx,
+                              float *topk_w, int32_t *expert_counts, int32_t *expert_offsets,
+                              int32_t *rank_counts, int32_t *rank_offsets, int32_t *send_counts,
+                              int32_t *pos, int32_t *status, void *packed_x, float *packed_scales,
+                              int32_t *packed_src, void *stream);
+
 /* Dispatch pack with fp8 block quantisation fused in.  Source: "Lower
  * latency and higher throughput with multi-node DeepSeek deployment",
  * section "Quantization" (activations quantised on the fly, one scaling
