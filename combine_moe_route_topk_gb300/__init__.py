@@ -30,6 +30,7 @@ MOE_ERR_TIMEOUT = -5
 
 MOE_BF16, MOE_F32, MOE_FP8E4M3_BLK128 = 0, 1, 2
 MOE_SOFTMAX, MOE_SIGMOID = 0, 1
+MOE_BIAS_SELECT_ONLY = 0x10  # OR into score_fn: the bias enters the selection key only
 
 STATUS_NAMES = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED",
                 -3: "MOE_ERR_CUDA", -4: "MOE_ERR_CAPACITY", -5: "MOE_ERR_TIMEOUT"}

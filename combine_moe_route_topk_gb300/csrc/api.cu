@@ -159,12 +159,17 @@ int moe_buffer_sizes(const MoeDims *dims, MoeSizes *out) {
     return MOE_OK;
 }
 
+static bool valid_score_fn(int score_fn) {
+    const int fn = score_fn & ~MOE_BIAS_SELECT_ONLY;
+    return fn == MOE_SOFTMAX || fn == MOE_SIGMOID;
+}
+
 int moe_route_topk(const MoeDims *dims, const float *logits, const float *bias, int score_fn,
                    int renormalize, int32_t *topk_idx, float *topk_w, void *stream) {
     Derived v;
     int rc = check_dims(dims, &v, "moe_route_topk");
     if (rc != MOE_OK) return rc;
-    if (score_fn != MOE_SOFTMAX && score_fn != MOE_SIGMOID)
+    if (!valid_score_fn(score_fn))
         return set_error(MOE_ERR_INVALID_ARG, "moe_route_topk: unknown score_fn %d", score_fn);
     if (v.NT == 0) return MOE_OK;
     if (!logits || !topk_idx || !topk_w)
@@ -349,7 +354,7 @@ int moe_dispatch_fused(const MoeDims *dims, const float *logits, const float *bi
     Derived v;
     int rc = check_dims(dims, &v, "moe_dispatch_fused");
     if (rc != MOE_OK) return rc;
-    if (score_fn != MOE_SOFTMAX && score_fn != MOE_SIGMOID)
+    if (!valid_score_fn(score_fn))
         return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_fused: unknown score_fn %d", score_fn);
     const char *why = fused_unsupported(dims->N, dims->T, dims->E, dims->R);
     if (why[0] != '\0')

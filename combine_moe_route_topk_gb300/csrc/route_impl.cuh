@@ -80,6 +80,38 @@ __device__ __forceinline__ void route_token(const float *__restrict__ logits,
         for (int j = 0; j < J; ++j)
             if (e0 + j < E) z[j] = __ldg(row + e0 + j);
     }
+    const bool softmax = (score_fn & ~MOE_BIAS_SELECT_ONLY) == MOE_SOFTMAX;
+    const bool bias_select = (score_fn & MOE_BIAS_SELECT_ONLY) != 0;
+    // Bias for selection only: the scores s_e come from the raw logits and
+    // the key is fl32(s_e + bias_e).  z[j] becomes s_j here; the bias is
+    // added below as in the default mode.  The same expressions recompute
+    // the winners' scores for the weights, so keys and weights agree.
+    float lmax = 0.f, lsum = 0.f;  // softmax statistics of the raw logits
+    if (bias_select) {
+        if (softmax) {
+            float m = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < J; ++j)
+                if (e0 + j < E) m = fmaxf(m, z[j]);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+            lmax = m;
+            float t = 0.f;
+#pragma unroll
+            for (int j = 0; j < J; ++j)
+                if (e0 + j < E) t += expf(__fsub_rn(z[j], lmax));
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(kFull, t, off);
+            lsum = t;
+#pragma unroll
+            for (int j = 0; j < J; ++j)
+                if (e0 + j < E) z[j] = __fdiv_rn(expf(__fsub_rn(z[j], lmax)), lsum);
+        } else {
+#pragma unroll
+            for (int j = 0; j < J; ++j)
+                if (e0 + j < E) z[j] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z[j])));
+        }
+    }
     // JP >= J slots (a power of two for the sorting network); padding
     // slots carry key 0 and sort last
     constexpr int JP = (J <= 1) ? 1 : (J <= 2) ? 2 : (J <= 4) ? 4 : (J <= 8) ? 8 : (J <= 16) ? 16 : 32;
@@ -134,7 +166,13 @@ __device__ __forceinline__ void route_token(const float *__restrict__ logits,
     }
 
     float p = 0.f;
-    if (score_fn == MOE_SOFTMAX) {
+    if (bias_select) {
+        if (lane < R) {
+            const float l = __ldg(row + my_e);
+            p = softmax ? __fdiv_rn(expf(__fsub_rn(l, lmax)), lsum)
+                        : __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l)));
+        }
+    } else if (softmax) {
         float s = 0.f;
 #pragma unroll
         for (int j = 0; j < J; ++j)

@@ -51,6 +51,10 @@ extern "C" {
 /* ---- router score functions --------------------------------------------- */
 #define MOE_SOFTMAX 0 /* softmax over all E experts, then top-R */
 #define MOE_SIGMOID 1 /* logistic sigmoid per expert */
+/* Flag OR'ed into score_fn: the bias takes part in the selection only (the
+ * DeepSeek-V3 router convention): scores s_e = score(logit_e), selection
+ * key fl32(s_e + bias_e), weights s_e of the selected experts. */
+#define MOE_BIAS_SELECT_ONLY 0x10
 
 /* Problem dimensions.  Limits: N >= 1, T >= 0, 1 <= E <= 1024, E % N == 0,
  * 1 <= R <= min(E, 32), H >= 8 and H % 8 == 0 (H % 128 == 0 for fp8 x),
@@ -107,13 +111,21 @@ int moe_buffer_sizes(const MoeDims *dims, MoeSizes *out);
  * serves DeepSeek- and Mixtral-style models).
  *   logits   f32 [N*T][E]            router logits
  *   bias     f32 [E] or NULL         per-expert bias added to every logit
- *   score_fn MOE_SOFTMAX | MOE_SIGMOID
+ *   score_fn MOE_SOFTMAX | MOE_SIGMOID, optionally | MOE_BIAS_SELECT_ONLY
  *   renormalize  nonzero: divide the selected scores by their sum
- *   topk_idx i32 [N*T][R] (out)      experts by key z = fl32(logit + bias)
- *                                    descending; equal keys -> lower index
+ *   topk_idx i32 [N*T][R] (out)      experts by key descending; equal keys
+ *                                    -> lower index.  Key z = fl32(logit +
+ *                                    bias); with MOE_BIAS_SELECT_ONLY the key
+ *                                    is fl32(s + bias), s = f32 score of the
+ *                                    raw logit
  *   topk_w   f32 [N*T][R] (out)      score of each selected expert
- * Scores are computed from z in f32 (softmax over all E).  Non-finite logits
- * give unspecified, but always in-range, selections. */
+ * Scores are computed in f32 (softmax over all E) from z, or from the raw
+ * logits with MOE_BIAS_SELECT_ONLY.  The pages do not say where the bias
+ * enters; adding it to the logit is the default reading.  With the flag,
+ * the selection is decided on f32 scores: keys within a few units in the
+ * last place of each other may order differently from an exact-arithmetic
+ * reference.  Non-finite logits give unspecified, but always in-range,
+ * selections. */
 int moe_route_topk(const MoeDims *dims, const float *logits, const float *bias, int score_fn,
                    int renormalize, int32_t *topk_idx, float *topk_w, void *stream);
 

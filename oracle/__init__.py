@@ -27,6 +27,7 @@ _lib = None
 
 OK, ERR_INVALID, ERR_CAPACITY = 0, -1, -4
 SOFTMAX, SIGMOID = 0, 1
+BIAS_SELECT_ONLY = 0x10  # flag OR'ed into score_fn: bias in the selection key only
 BF16, F32, FP8 = 0, 1, 2
 EXPERT_OPS = {"identity": 0, "scale": 1, "dequant": 2}
 

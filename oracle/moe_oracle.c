@@ -35,6 +35,7 @@
 
 #define OR_SOFTMAX 0
 #define OR_SIGMOID 1
+#define OR_BIAS_SELECT_ONLY 0x10 /* flag OR'ed into score_fn, see step 1 */
 
 #define OR_BF16 0
 #define OR_F32 1
@@ -151,6 +152,13 @@ uint16_t oracle_f32_to_bf16(float f) { return f32_to_bf16(f); }
  * E experts (p_e = exp(z_e - max z) / sum_j exp(z_j - max z)) or the
  * logistic sigmoid p_e = 1 / (1 + exp(-z_e)).  Optional renormalisation
  * divides the selected p by their sum.  Weights are rounded to float once.
+ *
+ * With OR_BIAS_SELECT_ONLY (the DeepSeek-V3 router convention; the pages
+ * do not say where the bias enters) the bias only moves the selection:
+ * s_e = score of the raw logit (softmax over all E, or sigmoid), the key is
+ * fl32(fl32(s_e) + bias_e) -- the selection is decided on float scores, as
+ * a float kernel decides it -- ties again towards the lower index, and the
+ * weights are the selected s_e (unrounded), optionally renormalised.
  * ------------------------------------------------------------------------ */
 
 static const float *g_sort_z; /* key array for the comparator (single thread) */
@@ -166,21 +174,43 @@ static int cmp_expert(const void *a, const void *b) {
 int oracle_route(int64_t NT, int E, int R, const float *logits, const float *bias,
                  int score_fn, int renorm, int32_t *topk_idx, float *topk_w,
                  double *topk_w64 /* nullable: unrounded weights */) {
-    if (E <= 0 || R <= 0 || R > E) return OR_ERR_INVALID;
+    const int bias_select = (score_fn & OR_BIAS_SELECT_ONLY) != 0;
+    const int fn = score_fn & ~OR_BIAS_SELECT_ONLY;
+    if (E <= 0 || R <= 0 || R > E || (fn != OR_SOFTMAX && fn != OR_SIGMOID)) return OR_ERR_INVALID;
     float *z = (float *)malloc(sizeof(float) * (size_t)E);
     int *order = (int *)malloc(sizeof(int) * (size_t)E);
     double *p = (double *)malloc(sizeof(double) * (size_t)R);
+    double *sc = (double *)malloc(sizeof(double) * (size_t)E); /* raw-logit scores */
     for (int64_t g = 0; g < NT; ++g) {
         const float *lg = logits + g * E;
+        if (bias_select) {
+            if (fn == OR_SOFTMAX) {
+                double lmax = (double)lg[0];
+                for (int e = 1; e < E; ++e)
+                    if ((double)lg[e] > lmax) lmax = (double)lg[e];
+                double denom = 0.0;
+                for (int e = 0; e < E; ++e) denom += exp((double)lg[e] - lmax);
+                for (int e = 0; e < E; ++e) sc[e] = exp((double)lg[e] - lmax) / denom;
+            } else {
+                for (int e = 0; e < E; ++e) sc[e] = 1.0 / (1.0 + exp(-(double)lg[e]));
+            }
+        }
         for (int e = 0; e < E; ++e) {
             float b = bias ? bias[e] : 0.0f;
-            z[e] = lg[e] + b; /* one correctly rounded float addition */
+            if (bias_select) {
+                float s_f = (float)sc[e];
+                z[e] = s_f + b; /* float score plus bias, one float addition */
+            } else {
+                z[e] = lg[e] + b; /* one correctly rounded float addition */
+            }
             order[e] = e;
         }
         g_sort_z = z;
         qsort(order, (size_t)E, sizeof(int), cmp_expert);
 
-        if (score_fn == OR_SOFTMAX) {
+        if (bias_select) {
+            for (int k = 0; k < R; ++k) p[k] = sc[order[k]];
+        } else if (fn == OR_SOFTMAX) {
             double zmax = (double)z[order[0]];
             double denom = 0.0;
             for (int e = 0; e < E; ++e) denom += exp((double)z[e] - zmax);
@@ -202,6 +232,7 @@ int oracle_route(int64_t NT, int E, int R, const float *logits, const float *bia
     free(z);
     free(order);
     free(p);
+    free(sc);
     return OR_OK;
 }
 

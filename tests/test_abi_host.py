@@ -145,6 +145,8 @@ def test_null_and_misaligned_pointers_are_rejected(lib):
     assert lib.moe_route_topk(ctypes.byref(d), odd, None, 0, 0, ok, ok, None) == E_INV
     assert lib.moe_route_topk(ctypes.byref(d), ok, None, 5, 0, ok, ok, None) == E_INV
     assert "score_fn" in lib.moe_last_error().decode()
+    for bad in (0x20, 0x12, moe.MOE_BIAS_SELECT_ONLY | 2, -1):
+        assert lib.moe_route_topk(ctypes.byref(d), ok, None, bad, 0, ok, ok, None) == E_INV
     assert lib.moe_dispatch_count(ctypes.byref(d), ok, ok, ok, ok, ok, ok, ok, None, None) == E_INV
     assert lib.moe_dispatch_pack(ctypes.byref(d), mis16, None, ok, ok, None, ok, None) == E_INV
     assert "16-byte" in lib.moe_last_error().decode()

@@ -18,7 +18,9 @@ from combine_moe_route_topk_gb300 import workloads as W
 
 from conftest import GOLDEN
 
-SCORE = {"softmax": oracle.SOFTMAX, "sigmoid": oracle.SIGMOID}
+SCORE = {"softmax": oracle.SOFTMAX, "sigmoid": oracle.SIGMOID,
+         "softmax_bias_select": oracle.SOFTMAX | oracle.BIAS_SELECT_ONLY,
+         "sigmoid_bias_select": oracle.SIGMOID | oracle.BIAS_SELECT_ONLY}
 
 
 def _golden(name):
@@ -87,6 +89,40 @@ def test_route_softmax_ratio_closed_form():
         # and the top weight against the full denominator
         den = np.exp(z[g] - z[g].max()).sum()
         assert w64[g, 0] == pytest.approx(1.0 / den, rel=1e-12)
+
+
+@pytest.mark.parametrize("fn", [oracle.SOFTMAX, oracle.SIGMOID])
+def test_route_bias_select_without_bias_is_the_default_reading(fn):
+    # scores are monotone in the logit, so with no bias the flag changes
+    # neither the selection nor (no bias to add) the weights
+    w = W.Workload("t", N=1, T=80, E=48, R=6, H=8, seed=11)
+    logits = W.make_inputs(w).logits.numpy()
+    a = oracle.route(logits, None, 6, fn, True)
+    b = oracle.route(logits, None, 6, fn | oracle.BIAS_SELECT_ONLY, True)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_allclose(a[2], b[2], rtol=1e-12, atol=0)
+
+
+def test_route_bias_select_weights_are_raw_scores():
+    # a bias of +100 forces a chosen set of experts into the selection; their
+    # weights stay the sigmoid / softmax of the raw logits (scipy's expit and
+    # softmax), which adding the bias to the logit would not give
+    special = pytest.importorskip("scipy.special")
+    w = W.Workload("t", N=1, T=50, E=32, R=4, H=8, seed=12)
+    logits = W.make_inputs(w).logits.numpy()
+    forced = [3, 17, 18, 30]
+    bias = np.zeros(32, np.float32)
+    bias[forced] = 100.0
+    for fn, ref in [(oracle.SIGMOID, special.expit(logits.astype(np.float64))),
+                    (oracle.SOFTMAX, special.softmax(logits.astype(np.float64), axis=1))]:
+        idx, _, w64 = oracle.route(logits, bias, 4, fn | oracle.BIAS_SELECT_ONLY, False)
+        assert all(sorted(r) == forced for r in idx.tolist())
+        np.testing.assert_allclose(w64, np.take_along_axis(ref, idx.astype(np.int64), 1),
+                                   rtol=1e-12, atol=0)
+        # and the selection order follows the float keys (float score + bias)
+        keys = ref.astype(np.float32) + bias
+        assert keys.dtype == np.float32
+        np.testing.assert_array_equal(idx, _lexsort_topk(keys, 4))
 
 
 def test_route_sigmoid_symmetry_and_monotone():
