@@ -302,19 +302,19 @@ def run_ours(args):
     def flush():
         torch.sum(flush_buf, dim=0, out=flush_out)
 
-    def launch(k):
+    def launch(k, s=None):
+        s = stream if s is None else s
         if k == "route":
             moe.route_topk(dims, inp.logits, inp.bias, w.score_fn, w.renormalize, b.topk_idx,
-                           b.topk_w, stream)
+                           b.topk_w, s)
         elif k == "count":
             moe.dispatch_count(dims, b.topk_idx, b.expert_counts, b.expert_offsets,
-                               b.rank_counts, b.rank_offsets, b.send_counts, b.pos, b.status,
-                               stream)
+                               b.rank_counts, b.rank_offsets, b.send_counts, b.pos, b.status, s)
         elif k == "pack":
             moe.dispatch_pack(dims, inp.x, inp.x_scales, b.pos, b.packed_x, b.packed_scales,
-                              b.packed_src, stream)
+                              b.packed_src, s)
         else:
-            moe.combine(dims, b.y, b.pos, b.topk_w, b.out, stream)
+            moe.combine(dims, b.y, b.pos, b.topk_w, b.out, s)
 
     def step(ev):
         # dispatch (route -> count -> pack) back to back, so each kernel's
@@ -394,6 +394,43 @@ def run_ours(args):
         per["combine"].append(ev[4].elapsed_time(ev[5]))
     per_timed = {"dispatch (route+count+pack)": statistics.mean(dispatch_ms),
                  "combine": statistics.mean(combine_ms)}
+
+    # the same step replayed from CUDA graphs, as a serving loop runs it:
+    # dispatch (route -> count -> pack, with their programmatic-dependency
+    # edges) and combine captured once each, the L2 flush between replays
+    cap_stream = torch.cuda.Stream(dev)
+    g_disp, g_comb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    cap_stream.wait_stream(stream)
+    with torch.cuda.graph(g_disp, stream=cap_stream):
+        for k in ("route", "count", "pack"):
+            launch(k, cap_stream)
+    with torch.cuda.graph(g_comb, stream=cap_stream):
+        launch("combine", cap_stream)
+    stream.wait_stream(cap_stream)
+    gevs = []
+    for i in range(args.steps + max(3, args.warmup)):
+        flush()
+        e = new_events(4)
+        e[0].record(stream)
+        g_disp.replay()
+        e[1].record(stream)
+        flush()
+        e[2].record(stream)
+        g_comb.replay()
+        e[3].record(stream)
+        if i >= max(3, args.warmup):
+            gevs.append(e)
+    torch.cuda.synchronize(dev)
+    if moe.read_status(b.status, stream) != moe.MOE_OK:
+        raise SystemExit("dispatch_count status after graph replays")
+    g_step = [e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in gevs]
+    g_ms = reduce_max(statistics.mean(g_step), pg)
+    graph_replay = {"ms_per_step": g_ms, "median_ms_per_step": statistics.median(g_step),
+                    "dispatch_ms": statistics.mean(e[0].elapsed_time(e[1]) for e in gevs),
+                    "combine_ms": statistics.mean(e[2].elapsed_time(e[3]) for e in gevs),
+                    "value": job_throughput(w.NT, world, g_ms), "replays": len(gevs),
+                    "note": "two CUDA graphs (dispatch, combine) replayed per step"}
+    del g_disp, g_comb
 
     # the quantising pack (bf16 rows -> e4m3 + per-128 scales), timed alone
     # on the same routing; it replaces pack when the experts take fp8 input
@@ -528,7 +565,9 @@ def run_ours(args):
         mean_ms = statistics.mean(per[k])
         kern[k] = {"ms": mean_ms, "median_ms": statistics.median(per[k]),
                    "alg_bytes": alg[k], "alg_gbs": alg[k] / (mean_ms / 1e3) / 1e9}
-    dom = max(("pack", "combine"), key=lambda k: kern[k]["ms"])
+    # the dominant kernel by median (a single stalled launch cannot flip it);
+    # its achieved rate below uses the mean launch time
+    dom = max(("pack", "combine"), key=lambda k: kern[k]["median_ms"])
     # combine has its own events inside the timed region; pack's come from
     # the breakdown pass right after it
     dom_ms = per_timed["combine"] if dom == "combine" else kern["pack"]["ms"]
@@ -559,6 +598,7 @@ def run_ours(args):
         "pack_plus_combine": {"ms": pc_ms, "alg_gbs": pc_gbs, "frac": pc_gbs / peak,
                               "frac_of_8tbs_nominal": pc_gbs / 8000.0},
         "timed_segments_ms": per_timed,
+        "graph_replay": graph_replay,
         "pack_quant": quant,
         "fused_dispatch": fused,
         "next_rows": next_rows,

@@ -32,6 +32,17 @@ int sm_count() {
     return sms;
 }
 
+int64_t l2_bytes() {
+    static thread_local int dev_cached = -1, l2 = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev != dev_cached) {
+        if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess) l2 = 0;
+        dev_cached = dev;
+    }
+    return l2;
+}
+
 namespace {
 
 constexpr int64_t kI32Max = 2147483647;
@@ -224,7 +235,7 @@ int moe_dispatch_pack(const MoeDims *dims, const void *x, const float *x_scales,
                                                      (cudaStream_t)stream),
                            "moe_dispatch_pack");
     return cuda_result(launch_dispatch_pack(x, fp8 ? x_scales : nullptr, pos, v.NT, dims->R, v.x_row_bytes,
-                                            v.scales_per_row, 0, v.rows_total, packed_x,
+                                            v.scales_per_row, 0, v.rows_total, 1, packed_x,
                                             fp8 ? packed_scales : nullptr, packed_src,
                                             (cudaStream_t)stream),
                        "moe_dispatch_pack");
@@ -286,7 +297,7 @@ int moe_dispatch_pack_rank(const MoeDims *dims, int rank, const void *x, const f
         return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_pack_rank: index and scale pointers must be 4-byte aligned");
     return cuda_result(launch_dispatch_pack(x, fp8 ? x_scales : nullptr, pos, v.NT, dims->R, v.x_row_bytes,
                                             v.scales_per_row, (int64_t)rank * v.cap, (int64_t)(rank + 1) * v.cap,
-                                            packed_x, fp8 ? packed_scales : nullptr, packed_src,
+                                            0, packed_x, fp8 ? packed_scales : nullptr, packed_src,
                                             (cudaStream_t)stream),
                        "moe_dispatch_pack_rank");
 }

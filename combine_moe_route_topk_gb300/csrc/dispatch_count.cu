@@ -120,6 +120,12 @@ dispatch_count_kernel(const int32_t *__restrict__ topk_idx, int N, int T, int E,
                                                 : kSendSmemAtomics;
     const bool one_tile = per <= kThreads;
 
+    // Dependents may be scheduled at once: the library's kernels that follow
+    // count read nothing before their own wait except L2 prefetch hints,
+    // which cannot return stale data, so pack can start pulling x into L2
+    // while route and count are still running.
+    grid_launch_dependents();
+
     // ---- phase 0: clear shared state (overlaps the previous kernel's tail)
     if (tid < kMaxCluster) sfirst_tab[tid] = (T > 0) ? min(NT, tid * per) / T : 0;
     for (int i = tid; i < 2 * E; i += kThreads) run[i] = 0;
@@ -370,7 +376,6 @@ dispatch_count_kernel(const int32_t *__restrict__ topk_idx, int N, int T, int E,
     // this block reads no remote shared memory after this point; it waits for
     // the others to say the same only before exiting
     asm volatile("barrier.cluster.arrive.release;" ::: "memory");
-    grid_launch_dependents();
 
     // exclusive scan of stot over experts: thread t sums the ipt consecutive
     // experts [t*ipt, t*ipt + ipt), then a two-level warp scan

@@ -17,6 +17,14 @@
 // times.  One block handles one token at a time; its threads move 16-byte
 // vectors (every row starts on a 16-byte boundary because H*elem % 16 == 0),
 // keeping all of their loads of a row in flight before issuing the R stores.
+//
+// Reads and writes are separated in time: the kernel is scheduled while
+// route and count (latency-bound, HBM nearly idle) still run, and its first
+// blocks use that time to pull the x rows into L2 with bulk prefetches
+// (evict-last) before they wait for count; the R-fold row stores carry an
+// evict-first hint so that they do not push those rows out again.  The
+// prefetch covers at most half of the L2, and is left out for a row window
+// (one rank's rows), which reads only some of the tokens.
 #include "moe_internal.cuh"
 #include "pdl.cuh"
 
@@ -34,30 +42,50 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
     return v;
 }
 
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void st_evict_first(uint4 *p, const uint4 &v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
+}
+
+// Bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16).
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes, uint64_t pol) {
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(p),
+                 "r"(bytes), "l"(pol)
+                 : "memory");
+}
+
 __global__ void __launch_bounds__(kPackThreads)
 dispatch_pack_kernel(const uint4 *__restrict__ x, const float *__restrict__ x_scales,
                      const int32_t *__restrict__ pos, int64_t NT, int R, int nvec, int spr,
-                     int64_t row_lo, int64_t row_hi, uint4 *__restrict__ packed_x,
-                     float *__restrict__ packed_scales, int32_t *__restrict__ packed_src) {
+                     int64_t row_lo, int64_t row_hi, int64_t pf_rows, int pf_blocks,
+                     uint4 *__restrict__ packed_x, float *__restrict__ packed_scales,
+                     int32_t *__restrict__ packed_src) {
     __shared__ int s_pos[32];
     const int tid = threadIdx.x;
-    // The first token's row is loaded before waiting for the previous kernel:
-    // x is not produced by the count kernel (only pos is), and every kernel
-    // of this library lets its dependents start only after its own inputs
-    // are final, so the row is complete here.  This overlaps the row load
-    // with the tail of the count kernel.
-    const int64_t g_first = blockIdx.x;
-    const bool preload = g_first < NT && nvec <= kPackThreads * kPackVecs;
-    uint4 pre[kPackVecs];
-    if (preload) {
-#pragma unroll
-        for (int u = 0; u < kPackVecs; ++u) {
-            const int c = tid + u * kPackThreads;
-            if (c < nvec) pre[u] = ld_stream(x + g_first * nvec + c);
-        }
+    // Rows [0, pf_rows) go to L2 ahead of use; block b < pf_blocks takes rows
+    // b, b + pf_blocks, ...  A prefetch is only a hint and L2 is where every
+    // write to x lands, so issuing it before the wait cannot yield stale data.
+    if (tid == 0 && (int)blockIdx.x < pf_blocks) {
+        const uint64_t keep = l2_policy_evict_last();
+        for (int64_t r = blockIdx.x; r < pf_rows; r += pf_blocks)
+            prefetch_l2(x + r * nvec, (uint32_t)nvec * 16u, keep);
     }
-    grid_dependency_wait();  // pos comes from the count kernel
+    grid_dependency_wait();  // pos comes from the count kernel (x may come from earlier ones)
     grid_launch_dependents();
+    const uint64_t stream_out = l2_policy_evict_first();
     for (int64_t g = blockIdx.x; g < NT; g += gridDim.x) {
         if (tid < R) {
             const int p = __ldg(pos + g * R + tid);
@@ -71,15 +99,10 @@ dispatch_pack_kernel(const uint4 *__restrict__ x, const float *__restrict__ x_sc
         const uint4 *src = x + g * nvec;
         for (int c0 = tid; any && c0 < nvec; c0 += kPackThreads * kPackVecs) {
             uint4 v[kPackVecs];
-            if (preload && g == g_first) {
 #pragma unroll
-                for (int u = 0; u < kPackVecs; ++u) v[u] = pre[u];
-            } else {
-#pragma unroll
-                for (int u = 0; u < kPackVecs; ++u) {
-                    const int c = c0 + u * kPackThreads;
-                    if (c < nvec) v[u] = ld_stream(src + c);
-                }
+            for (int u = 0; u < kPackVecs; ++u) {
+                const int c = c0 + u * kPackThreads;
+                if (c < nvec) v[u] = ld_stream(src + c);
             }
             for (int k = 0; k < R; ++k) {
                 const int p = s_pos[k];
@@ -88,7 +111,7 @@ dispatch_pack_kernel(const uint4 *__restrict__ x, const float *__restrict__ x_sc
 #pragma unroll
                 for (int u = 0; u < kPackVecs; ++u) {
                     const int c = c0 + u * kPackThreads;
-                    if (c < nvec) dst[c] = v[u];
+                    if (c < nvec) st_evict_first(dst + c, v[u], stream_out);
                 }
             }
         }
@@ -107,11 +130,18 @@ dispatch_pack_kernel(const uint4 *__restrict__ x, const float *__restrict__ x_sc
 
 cudaError_t launch_dispatch_pack(const void *x, const float *x_scales, const int32_t *pos,
                                  int64_t NT, int R, int64_t row_bytes, int scales_per_row,
-                                 int64_t row_lo, int64_t row_hi, void *packed_x,
+                                 int64_t row_lo, int64_t row_hi, int prefetch_x, void *packed_x,
                                  float *packed_scales, int32_t *packed_src, cudaStream_t stream) {
     if (NT == 0) return cudaSuccess;
     const int nvec = (int)(row_bytes / 16);
     const int64_t grid = NT < (int64_t)0x7fffffff ? NT : (int64_t)0x7fffffff;
+    // prefetch (whole dispatch only): rows filling at most half the L2,
+    // issued by one block per SM
+    int64_t pf_rows = (prefetch_x && row_bytes <= 65536) ? (l2_bytes() / 2) / row_bytes : 0;
+    if (pf_rows > NT) pf_rows = NT;
+    int64_t pf_blocks = sm_count();
+    if (pf_blocks > grid) pf_blocks = grid;
+    if (pf_rows <= 0 || pf_blocks <= 0) pf_rows = pf_blocks = 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kPackThreads);
@@ -121,7 +151,8 @@ cudaError_t launch_dispatch_pack(const void *x, const float *x_scales, const int
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, dispatch_pack_kernel, reinterpret_cast<const uint4 *>(x),
                               x_scales, pos, NT, R, nvec, scales_per_row, row_lo, row_hi,
-                              reinterpret_cast<uint4 *>(packed_x), packed_scales, packed_src);
+                              pf_rows, (int)pf_blocks, reinterpret_cast<uint4 *>(packed_x),
+                              packed_scales, packed_src);
 }
 
 }  // namespace moe

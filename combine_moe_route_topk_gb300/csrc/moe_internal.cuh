@@ -14,6 +14,7 @@ int set_error(int code, const char *fmt, ...);
 
 // Multiprocessor count of the current device (cached per device).
 int sm_count();
+int64_t l2_bytes();  // L2 cache size of the current device (0 if unknown)
 
 // ---- launchers (arguments already validated by the C entry points) -------
 
@@ -30,7 +31,7 @@ cudaError_t launch_dispatch_count(const int32_t *topk_idx, int N, int T, int E, 
 // Pairs whose row lies outside [row_lo, row_hi) are skipped.
 cudaError_t launch_dispatch_pack(const void *x, const float *x_scales, const int32_t *pos,
                                  int64_t NT, int R, int64_t row_bytes, int scales_per_row,
-                                 int64_t row_lo, int64_t row_hi, void *packed_x,
+                                 int64_t row_lo, int64_t row_hi, int prefetch_x, void *packed_x,
                                  float *packed_scales, int32_t *packed_src, cudaStream_t stream);
 
 // Bulk-copy pack (whole rows through shared memory); rows of more than

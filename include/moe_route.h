@@ -169,12 +169,10 @@ int moe_dispatch_count(const MoeDims *dims, const int32_t *topk_idx, int32_t *ex
  *   packed_src    i32 [N*cap] (out): row pos[g][k] = g*R + k
  * Only rows [d*cap, d*cap + min(rank_counts[d], cap)) of each region are
  * written; pairs with pos < 0 (or outside [0, N*cap)) are skipped.
- * Ordering: like every kernel here, pack waits for the previous kernel in
- * the stream before reading pos, but it may read x while that kernel is
- * still finishing if that kernel allows programmatic dependent launch (the
- * library's kernels do, after their own inputs are final, and none of them
- * writes x).  A caller whose own kernel writes x right before pack and
- * triggers programmatic launch early must not do so before x is final. */
+ * Ordering: like every kernel here, pack reads its inputs only after the
+ * previous kernel in the stream has completed.  Before that it may issue L2
+ * prefetches of x (hints only, which never return stale data) so that the
+ * rows are on chip by the time count finishes. */
 int moe_dispatch_pack(const MoeDims *dims, const void *x, const float *x_scales,
                       const int32_t *pos, void *packed_x, float *packed_scales,
                       int32_t *packed_src, void *stream);
