@@ -18,6 +18,7 @@
 // in flight at once, as in the plain combine.
 #include <cuda_bf16.h>
 
+#include "mem_ops.cuh"
 #include "moe_internal.cuh"
 #include "pdl.cuh"
 
@@ -27,14 +28,6 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kU = 1;   // output vectors per thread per pass
 constexpr int kKB = 8;  // source rows loaded together
-
-__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
 
 template <int kBf16>
 struct Vec;

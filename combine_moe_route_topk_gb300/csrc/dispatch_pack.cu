@@ -28,6 +28,7 @@
 // evict-first hint so that they do not push those rows out again.  The
 // prefetch covers at most half of the L2, and is left out for a row window
 // (one rank's rows), which reads only some of the tokens.
+#include "mem_ops.cuh"
 #include "moe_internal.cuh"
 #include "pdl.cuh"
 
@@ -37,39 +38,6 @@ namespace {
 constexpr int kPackVecs = 2;          // 16-byte vectors of a row per thread
 constexpr int kPackMaxThreads = 1024;
 
-__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-
-__device__ __forceinline__ void st_evict_first(uint4 *p, const uint4 &v, uint64_t pol) {
-    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "r"(v.x),
-                 "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
-                 : "memory");
-}
-
-// Bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16).
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes, uint64_t pol) {
-    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(p),
-                 "r"(bytes), "l"(pol)
-                 : "memory");
-}
-
 __global__ void __launch_bounds__(kPackMaxThreads)
 dispatch_pack_kernel(const uint4 *__restrict__ x, const float *__restrict__ x_scales,
                      const int32_t *__restrict__ pos, int64_t NT, int R, int nvec, int spr,
@@ -78,14 +46,7 @@ dispatch_pack_kernel(const uint4 *__restrict__ x, const float *__restrict__ x_sc
                      int32_t *__restrict__ packed_src) {
     __shared__ int s_pos[32];
     const int tid = threadIdx.x, nthr = blockDim.x;  // nthr >= 32 >= R
-    // Rows [0, pf_rows) go to L2 ahead of use; block b < pf_blocks takes rows
-    // b, b + pf_blocks, ...  A prefetch is only a hint and L2 is where every
-    // write to x lands, so issuing it before the wait cannot yield stale data.
-    if (tid == 0 && (int)blockIdx.x < pf_blocks) {
-        const uint64_t keep = l2_policy_evict_last();
-        for (int64_t r = blockIdx.x; r < pf_rows; r += pf_blocks)
-            prefetch_l2(x + r * nvec, (uint32_t)nvec * 16u, keep);
-    }
+    prefetch_rows_l2(x, (int64_t)nvec * 16, pf_rows, pf_blocks);  // before the wait: hints only
     grid_dependency_wait();  // pos comes from the count kernel (x may come from earlier ones)
     grid_launch_dependents();
     const uint64_t stream_out = l2_policy_evict_first();
