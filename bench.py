@@ -17,6 +17,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -90,9 +91,20 @@ def measured_peaks():
 
 
 def source_hash(name: str) -> str:
-    path = os.path.join(ROOT, "combine_moe_route_topk_gb300", "csrc", name)
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of a kernel source file and every local header it includes."""
+    csrc = os.path.join(ROOT, "combine_moe_route_topk_gb300", "csrc")
+    h = hashlib.sha256()
+    todo, seen = [name], set()
+    while todo:
+        f = todo.pop(0)
+        if f in seen or not os.path.exists(os.path.join(csrc, f)):
+            continue
+        seen.add(f)
+        with open(os.path.join(csrc, f), "rb") as fh:
+            data = fh.read()
+        h.update(f.encode() + b"\0" + data)
+        todo += [m.decode() for m in re.findall(rb'#include "([^"]+)"', data)]
+    return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel: str, workload: str):
