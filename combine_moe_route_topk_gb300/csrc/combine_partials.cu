@@ -35,7 +35,7 @@ struct Vec;
 template <>
 struct Vec<1> {  // 8 x bf16
     static constexpr int kElems = 8;
-    __device__ static void fma(float (&a)[8], float w, const uint4 &v) {
+    __device__ __forceinline__ static void fma(float (&a)[8], float w, const uint4 &v) {
         const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -43,8 +43,8 @@ struct Vec<1> {  // 8 x bf16
             a[2 * i + 1] = fmaf(w, __uint_as_float(u[i] & 0xffff0000u), a[2 * i + 1]);
         }
     }
-    __device__ static void add(float (&a)[8], const uint4 &v) { fma(a, 1.0f, v); }
-    __device__ static uint4 pack(const float (&a)[8]) {
+    __device__ __forceinline__ static void add(float (&a)[8], const uint4 &v) { fma(a, 1.0f, v); }
+    __device__ __forceinline__ static uint4 pack(const float (&a)[8]) {
         uint32_t u[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -58,25 +58,28 @@ struct Vec<1> {  // 8 x bf16
 template <>
 struct Vec<0> {  // 4 x f32
     static constexpr int kElems = 4;
-    __device__ static void fma(float (&a)[4], float w, const uint4 &v) {
+    __device__ __forceinline__ static void fma(float (&a)[4], float w, const uint4 &v) {
         a[0] = fmaf(w, __uint_as_float(v.x), a[0]);
         a[1] = fmaf(w, __uint_as_float(v.y), a[1]);
         a[2] = fmaf(w, __uint_as_float(v.z), a[2]);
         a[3] = fmaf(w, __uint_as_float(v.w), a[3]);
     }
-    __device__ static void add(float (&a)[4], const uint4 &v) {
+    __device__ __forceinline__ static void add(float (&a)[4], const uint4 &v) {
         a[0] += __uint_as_float(v.x);
         a[1] += __uint_as_float(v.y);
         a[2] += __uint_as_float(v.z);
         a[3] += __uint_as_float(v.w);
     }
-    __device__ static uint4 pack(const float (&a)[4]) {
+    __device__ __forceinline__ static uint4 pack(const float (&a)[4]) {
         return make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
                           __float_as_uint(a[3]));
     }
 };
 
-template <int kBf16>
+// kFew: R <= 8 (every row of a token loaded at once); else the rows of one
+// slot at a time.  Separate instances keep the rare path from perturbing
+// the register allocation of the common one.
+template <int kBf16, bool kFew>
 __global__ void __launch_bounds__(kThreads)
 combine_partials_kernel(const uint4 *__restrict__ y, const int32_t *__restrict__ pos,
                         const float *__restrict__ topk_w, int64_t NT, int R, int nvec, int64_t cap,
@@ -86,80 +89,130 @@ combine_partials_kernel(const uint4 *__restrict__ y, const int32_t *__restrict__
     constexpr int EL = V::kElems;
     __shared__ int s_pos[32], s_slot[32];
     __shared__ float s_w[32];
+    // the same pairs stably ordered by slot (invalid pairs last)
+    __shared__ int o_pos[32], o_slot[32];
+    __shared__ float o_w[32];
     __shared__ int s_nslot;
     const int tid = threadIdx.x;
     grid_dependency_wait();  // y, pos and topk_w come from earlier kernels
     grid_launch_dependents();
     for (int64_t g = blockIdx.x; g < NT; g += gridDim.x) {
-        if (tid < R) {
-            int p = __ldg(pos + g * R + tid);
-            s_pos[tid] = (p >= 0 && (int64_t)p < rows_total) ? p : -1;
-            s_w[tid] = __ldg(topk_w + g * R + tid);
-        }
-        __syncthreads();
-        if (tid == 0) {
-            // slots: the token's distinct ranks in the order of their first pair
-            int ranks[32];
-            int nslot = 0;
-            for (int k = 0; k < R; ++k) {
-                const int p = s_pos[k];
-                if (p < 0) {
-                    s_slot[k] = -1;
-                    continue;
-                }
-                const int d = (int)((int64_t)p / cap);
-                int j = 0;
-                while (j < nslot && ranks[j] != d) ++j;
-                if (j == nslot && nslot < P) ranks[nslot++] = d;
-                s_slot[k] = (j < nslot) ? j : -1;
+        if (tid < 32) {
+            // Warp 0, lane k = pair k: slots are the token's distinct ranks in
+            // the order of their first pair.  A lane's rank d = p / cap (32-bit:
+            // N * cap < 2^31 is checked on the host); lanes that share d form
+            // one match group whose lowest lane is its first pair, and the
+            // slot is the number of first pairs before that one.
+            const unsigned lane_bit = 1u << tid;
+            int p = -1;
+            float wk = 0.f;
+            if (tid < R) {
+                p = __ldg(pos + g * R + tid);
+                if (p < 0 || (int64_t)p >= rows_total) p = -1;
+                wk = __ldg(topk_w + g * R + tid);
             }
-            for (int j = 0; j < P; ++j) slot_rank[g * P + j] = (j < nslot) ? ranks[j] : -1;
-            s_nslot = nslot;
+            const bool valid = p >= 0;
+            // invalid lanes get a key of their own, so they match nobody
+            const int d = valid ? (int)((unsigned)p / (unsigned)cap) : -1 - tid;
+            const unsigned same = __match_any_sync(0xffffffffu, d);
+            const int first = __ffs(same) - 1;
+            const unsigned firsts = __ballot_sync(0xffffffffu, valid && first == tid);
+            const int slot = valid ? __popc(firsts & ((1u << first) - 1u)) : -1;
+            const int nslot = __popc(firsts);  // <= min(R, N) = P
+            // Position of pair k in the by-slot order: the pairs of earlier
+            // slots (group sizes summed over the first pairs below this
+            // pair's first pair, by an exclusive warp scan) plus the pairs of
+            // its own slot below it; invalid pairs go after all valid ones.
+            const unsigned below = lane_bit - 1u;
+            const int gsize = (valid && first == tid) ? __popc(same) : 0;
+            int incl = gsize;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, incl, off);
+                if (tid >= off) incl += t;
+            }
+            const int before_first = __shfl_sync(0xffffffffu, incl - gsize, first);
+            const unsigned valid_mask = __ballot_sync(0xffffffffu, valid);
+            const unsigned invalid_mask = __ballot_sync(0xffffffffu, tid < R && !valid);
+            const int order = valid ? before_first + __popc(same & below)
+                                    : __popc(valid_mask) + __popc(invalid_mask & below);
+            if (tid < R) {
+                s_pos[tid] = p;
+                s_w[tid] = wk;
+                s_slot[tid] = slot;
+                o_pos[order] = p;
+                o_w[order] = wk;
+                o_slot[order] = slot;
+            }
+            if (valid && (firsts & lane_bit)) slot_rank[g * P + slot] = d;
+            if (tid >= nslot && tid < P) slot_rank[g * P + tid] = -1;
+            if (tid == 0) s_nslot = nslot;
         }
         __syncthreads();
         const int nslot = s_nslot;
         for (int c0 = tid; c0 < nvec; c0 += kThreads * kU) {
-            // R <= 8: every row of the token is loaded once, up front
-            uint4 v[kKB][kU];
-            if (R <= kKB) {
+            if constexpr (kFew) {
+                // R <= 8: the token's rows are loaded once, up front, in slot
+                // order; one pass sums each slot's run of pairs (in k order)
+                // and stores its partial row where the run ends.
+                uint4 v[kKB][kU];
 #pragma unroll
-                for (int kk = 0; kk < kKB; ++kk) {
-                    const int p = (kk < R) ? s_pos[kk] : -1;
+                for (int i = 0; i < kKB; ++i) {
+                    const int p = (i < R) ? o_pos[i] : -1;
 #pragma unroll
                     for (int u = 0; u < kU; ++u) {
                         const int c = c0 + u * kThreads;
-                        v[kk][u] = (p >= 0 && c < nvec) ? ld_stream(y + (int64_t)p * nvec + c)
-                                                        : make_uint4(0u, 0u, 0u, 0u);
+                        v[i][u] = (p >= 0 && c < nvec) ? ld_stream(y + (int64_t)p * nvec + c)
+                                                       : make_uint4(0u, 0u, 0u, 0u);
                     }
                 }
-            }
+                float acc[kU][EL];
+#pragma unroll
+                for (int u = 0; u < kU; ++u)
+#pragma unroll
+                    for (int e = 0; e < EL; ++e) acc[u][e] = 0.f;
+#pragma unroll
+                for (int i = 0; i < kKB; ++i) {
+                    const int sl = (i < R) ? o_slot[i] : -1;  // invalid pairs sit at the end
+                    if (sl >= 0) {
+#pragma unroll
+                        for (int u = 0; u < kU; ++u) V::fma(acc[u], o_w[i], v[i][u]);
+                        const int next = (i + 1 < R) ? o_slot[i + 1] : -1;
+                        if (next != sl) {
+#pragma unroll
+                            for (int u = 0; u < kU; ++u) {
+                                const int c = c0 + u * kThreads;
+                                if (c < nvec) partial[(g * P + sl) * nvec + c] = V::pack(acc[u]);
+#pragma unroll
+                                for (int e = 0; e < EL; ++e) acc[u][e] = 0.f;
+                            }
+                        }
+                    }
+                }
+                for (int j = nslot; j < P; ++j) {
+#pragma unroll
+                    for (int u = 0; u < kU; ++u) {
+                        const int c = c0 + u * kThreads;
+                        if (c < nvec) partial[(g * P + j) * nvec + c] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+            } else {
+            // R > 8: the rows of one slot at a time
             for (int j = 0; j < P; ++j) {
                 float acc[kU][EL];
 #pragma unroll
                 for (int u = 0; u < kU; ++u)
 #pragma unroll
-                    for (int i = 0; i < EL; ++i) acc[u][i] = 0.f;
+                    for (int e = 0; e < EL; ++e) acc[u][e] = 0.f;
                 if (j < nslot) {
-                    if (R <= kKB) {
+                    for (int k = 0; k < R; ++k) {
+                        if (s_slot[k] != j) continue;
+                        const int p = s_pos[k];
+                        const float w = s_w[k];
 #pragma unroll
-                        for (int kk = 0; kk < kKB; ++kk) {
-                            if (kk < R && s_slot[kk] == j) {
-                                const float w = s_w[kk];
-#pragma unroll
-                                for (int u = 0; u < kU; ++u) V::fma(acc[u], w, v[kk][u]);
-                            }
-                        }
-                    } else {
-                        // R > 8: the rows of one slot at a time
-                        for (int k = 0; k < R; ++k) {
-                            if (s_slot[k] != j) continue;
-                            const int p = s_pos[k];
-                            const float w = s_w[k];
-#pragma unroll
-                            for (int u = 0; u < kU; ++u) {
-                                const int c = c0 + u * kThreads;
-                                if (c < nvec) V::fma(acc[u], w, ld_stream(y + (int64_t)p * nvec + c));
-                            }
+                        for (int u = 0; u < kU; ++u) {
+                            const int c = c0 + u * kThreads;
+                            if (c < nvec) V::fma(acc[u], w, ld_stream(y + (int64_t)p * nvec + c));
                         }
                     }
                 }
@@ -169,12 +222,14 @@ combine_partials_kernel(const uint4 *__restrict__ y, const int32_t *__restrict__
                     if (c < nvec) partial[(g * P + j) * nvec + c] = V::pack(acc[u]);
                 }
             }
+            }
         }
         __syncthreads();
     }
 }
 
-template <int kBf16>
+// kFew: P <= 8 (all partial rows of a token loaded at once)
+template <int kBf16, bool kFew>
 __global__ void __launch_bounds__(kThreads)
 reduce_partials_kernel(const uint4 *__restrict__ partial, const int32_t *__restrict__ slot_rank,
                        int64_t NT, int P, int nvec, uint4 *__restrict__ out) {
@@ -193,12 +248,31 @@ reduce_partials_kernel(const uint4 *__restrict__ partial, const int32_t *__restr
             for (int u = 0; u < kU; ++u)
 #pragma unroll
                 for (int i = 0; i < EL; ++i) acc[u][i] = 0.f;
-            for (int j = 0; j < P; ++j) {
-                if (!s_used[j]) continue;
+            if constexpr (kFew) {
+                // all used partial rows loaded first, then summed in slot order
+                uint4 v[kKB][kU];
 #pragma unroll
-                for (int u = 0; u < kU; ++u) {
-                    const int c = c0 + u * kThreads;
-                    if (c < nvec) V::add(acc[u], ld_stream(partial + (g * P + j) * nvec + c));
+                for (int j = 0; j < kKB; ++j)
+#pragma unroll
+                    for (int u = 0; u < kU; ++u) {
+                        const int c = c0 + u * kThreads;
+                        v[j][u] = (j < P && s_used[j] && c < nvec)
+                                      ? ld_stream(partial + (g * P + j) * nvec + c)
+                                      : make_uint4(0u, 0u, 0u, 0u);
+                    }
+#pragma unroll
+                for (int j = 0; j < kKB; ++j)
+                    if (j < P && s_used[j])
+#pragma unroll
+                        for (int u = 0; u < kU; ++u) V::add(acc[u], v[j][u]);
+            } else {
+                for (int j = 0; j < P; ++j) {
+                    if (!s_used[j]) continue;
+#pragma unroll
+                    for (int u = 0; u < kU; ++u) {
+                        const int c = c0 + u * kThreads;
+                        if (c < nvec) V::add(acc[u], ld_stream(partial + (g * P + j) * nvec + c));
+                    }
                 }
             }
 #pragma unroll
@@ -232,7 +306,9 @@ cudaError_t launch_combine_partials(const void *y, int y_dtype, const int32_t *p
     const int nvec = (int)((int64_t)H * (y_dtype == MOE_BF16 ? 2 : 4) / 16);
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = grid_cfg(NT, stream, attr);
-    auto kern = (y_dtype == MOE_BF16) ? combine_partials_kernel<1> : combine_partials_kernel<0>;
+    const bool few = R <= kKB;
+    auto kern = (y_dtype == MOE_BF16) ? (few ? combine_partials_kernel<1, true> : combine_partials_kernel<1, false>)
+                                      : (few ? combine_partials_kernel<0, true> : combine_partials_kernel<0, false>);
     return cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const uint4 *>(y), pos, topk_w, NT, R,
                               nvec, cap, rows_total, P, reinterpret_cast<uint4 *>(partial),
                               slot_rank);
@@ -244,7 +320,9 @@ cudaError_t launch_reduce_partials(const void *partial, int y_dtype, const int32
     const int nvec = (int)((int64_t)H * (y_dtype == MOE_BF16 ? 2 : 4) / 16);
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = grid_cfg(NT, stream, attr);
-    auto kern = (y_dtype == MOE_BF16) ? reduce_partials_kernel<1> : reduce_partials_kernel<0>;
+    const bool few = P <= kKB;
+    auto kern = (y_dtype == MOE_BF16) ? (few ? reduce_partials_kernel<1, true> : reduce_partials_kernel<1, false>)
+                                      : (few ? reduce_partials_kernel<0, true> : reduce_partials_kernel<0, false>);
     return cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const uint4 *>(partial), slot_rank, NT,
                               P, nvec, reinterpret_cast<uint4 *>(out));
 }
