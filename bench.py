@@ -406,6 +406,18 @@ def run_ours(args):
         flush()
         step_breakdown(bevs[i])
     torch.cuda.synchronize(dev)
+    # route -> count back to back (with PDL, as in the step): what the
+    # dispatch segment spends before pack's own work
+    rcpool = [new_events(2) for _ in range(nb)]
+    host_lead(nb)
+    for i in range(nb):
+        flush()
+        rcpool[i][0].record(stream)
+        launch("route")
+        launch("count")
+        rcpool[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    route_count_chain_ms = statistics.mean(a.elapsed_time(c) for a, c in rcpool)
     per = {k: [] for k in KERNELS}
     for ev in bevs:
         per["route"].append(ev[0].elapsed_time(ev[1]))
@@ -413,7 +425,8 @@ def run_ours(args):
         per["pack"].append(ev[2].elapsed_time(ev[3]))
         per["combine"].append(ev[4].elapsed_time(ev[5]))
     per_timed = {"dispatch (route+count+pack)": statistics.mean(dispatch_ms),
-                 "combine": statistics.mean(combine_ms)}
+                 "combine": statistics.mean(combine_ms),
+                 "route+count alone, back to back (diagnostic)": route_count_chain_ms}
 
     # the same step replayed from CUDA graphs, as a serving loop runs it:
     # dispatch (route -> count -> pack, with their programmatic-dependency

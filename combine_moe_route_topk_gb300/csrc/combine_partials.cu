@@ -26,7 +26,8 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kU = 1;   // output vectors per thread per pass
+constexpr int kU = 1;     // output vectors per thread per pass (partials)
+constexpr int kRedU = 2;  // output vectors per thread per pass (reduction)
 constexpr int kKB = 8;  // source rows loaded together
 
 template <int kBf16>
@@ -242,19 +243,19 @@ reduce_partials_kernel(const uint4 *__restrict__ partial, const int32_t *__restr
     for (int64_t g = blockIdx.x; g < NT; g += gridDim.x) {
         if (tid < P) s_used[tid] = __ldg(slot_rank + g * P + tid) >= 0;
         __syncthreads();
-        for (int c0 = tid; c0 < nvec; c0 += kThreads * kU) {
-            float acc[kU][EL];
+        for (int c0 = tid; c0 < nvec; c0 += kThreads * kRedU) {
+            float acc[kRedU][EL];
 #pragma unroll
-            for (int u = 0; u < kU; ++u)
+            for (int u = 0; u < kRedU; ++u)
 #pragma unroll
                 for (int i = 0; i < EL; ++i) acc[u][i] = 0.f;
             if constexpr (kFew) {
                 // all used partial rows loaded first, then summed in slot order
-                uint4 v[kKB][kU];
+                uint4 v[kKB][kRedU];
 #pragma unroll
                 for (int j = 0; j < kKB; ++j)
 #pragma unroll
-                    for (int u = 0; u < kU; ++u) {
+                    for (int u = 0; u < kRedU; ++u) {
                         const int c = c0 + u * kThreads;
                         v[j][u] = (j < P && s_used[j] && c < nvec)
                                       ? ld_stream(partial + (g * P + j) * nvec + c)
@@ -264,19 +265,19 @@ reduce_partials_kernel(const uint4 *__restrict__ partial, const int32_t *__restr
                 for (int j = 0; j < kKB; ++j)
                     if (j < P && s_used[j])
 #pragma unroll
-                        for (int u = 0; u < kU; ++u) V::add(acc[u], v[j][u]);
+                        for (int u = 0; u < kRedU; ++u) V::add(acc[u], v[j][u]);
             } else {
                 for (int j = 0; j < P; ++j) {
                     if (!s_used[j]) continue;
 #pragma unroll
-                    for (int u = 0; u < kU; ++u) {
+                    for (int u = 0; u < kRedU; ++u) {
                         const int c = c0 + u * kThreads;
                         if (c < nvec) V::add(acc[u], ld_stream(partial + (g * P + j) * nvec + c));
                     }
                 }
             }
 #pragma unroll
-            for (int u = 0; u < kU; ++u) {
+            for (int u = 0; u < kRedU; ++u) {
                 const int c = c0 + u * kThreads;
                 if (c < nvec) out[g * nvec + c] = V::pack(acc[u]);
             }
