@@ -295,10 +295,10 @@ int moe_dispatch_pack_rank(const MoeDims *dims, int rank, const void *x, const f
         return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_pack_rank: x and packed_x must be 16-byte aligned");
     if (!aligned(pos, 4) || !aligned(packed_src, 4) || (fp8 && (!aligned(x_scales, 4) || !aligned(packed_scales, 4))))
         return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_pack_rank: index and scale pointers must be 4-byte aligned");
-    return cuda_result(launch_dispatch_pack(x, fp8 ? x_scales : nullptr, pos, v.NT, dims->R, v.x_row_bytes,
-                                            v.scales_per_row, (int64_t)rank * v.cap, (int64_t)(rank + 1) * v.cap,
-                                            0, packed_x, fp8 ? packed_scales : nullptr, packed_src,
-                                            (cudaStream_t)stream),
+    return cuda_result(launch_pack_rank(x, fp8 ? x_scales : nullptr, pos, v.NT, dims->R, v.x_row_bytes,
+                                        v.scales_per_row, (int64_t)rank * v.cap, (int64_t)(rank + 1) * v.cap,
+                                        packed_x, fp8 ? packed_scales : nullptr, packed_src,
+                                        (cudaStream_t)stream),
                        "moe_dispatch_pack_rank");
 }
 
@@ -316,9 +316,9 @@ int moe_combine_rank(const MoeDims *dims, int rank, const void *y, const int32_t
         return set_error(MOE_ERR_INVALID_ARG, "moe_combine_rank: y and out must be 16-byte aligned");
     if (!aligned(pos, 4) || !aligned(topk_w, 4))
         return set_error(MOE_ERR_INVALID_ARG, "moe_combine_rank: pos and topk_w must be 4-byte aligned");
-    return cuda_result(launch_combine(y, dims->y_dtype, pos, topk_w, v.NT, dims->R, dims->H,
-                                      (int64_t)rank * v.cap, (int64_t)(rank + 1) * v.cap, out,
-                                      (cudaStream_t)stream),
+    return cuda_result(launch_combine_rank(y, dims->y_dtype, pos, topk_w, v.NT, dims->R, dims->H,
+                                           (int64_t)rank * v.cap, (int64_t)(rank + 1) * v.cap, out,
+                                           (cudaStream_t)stream),
                        "moe_combine_rank");
 }
 

@@ -16,11 +16,10 @@
 // token at a time; every thread owns 16-byte output vectors and issues the
 // loads of all R source rows (up to 8 at once) before accumulating them in
 // k order, so each thread keeps 8 x 2 x 16 bytes in flight.
-#include <cuda_bf16.h>
-
 #include "mem_ops.cuh"
 #include "moe_internal.cuh"
 #include "pdl.cuh"
+#include "vec_traits.cuh"
 
 namespace moe {
 namespace {
@@ -30,53 +29,11 @@ constexpr int kCombU = 2;   // output vectors per thread per pass
 constexpr int kCombKB = 8;  // source rows loaded together
 
 template <int kBf16>
-struct VecTraits;
-
-template <>
-struct VecTraits<1> {  // 8 x bf16 per 16 bytes
-    static constexpr int kElems = 8;
-    __device__ static void fma(float (&acc)[8], float w, const uint4 &v) {
-        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float lo = __uint_as_float(u[i] << 16);
-            const float hi = __uint_as_float(u[i] & 0xffff0000u);
-            acc[2 * i] = fmaf(w, lo, acc[2 * i]);
-            acc[2 * i + 1] = fmaf(w, hi, acc[2 * i + 1]);
-        }
-    }
-    __device__ static uint4 pack(const float (&acc)[8]) {
-        uint32_t u[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-            u[i] = *reinterpret_cast<const uint32_t *>(&h);
-        }
-        return make_uint4(u[0], u[1], u[2], u[3]);
-    }
-};
-
-template <>
-struct VecTraits<0> {  // 4 x f32 per 16 bytes
-    static constexpr int kElems = 4;
-    __device__ static void fma(float (&acc)[4], float w, const uint4 &v) {
-        acc[0] = fmaf(w, __uint_as_float(v.x), acc[0]);
-        acc[1] = fmaf(w, __uint_as_float(v.y), acc[1]);
-        acc[2] = fmaf(w, __uint_as_float(v.z), acc[2]);
-        acc[3] = fmaf(w, __uint_as_float(v.w), acc[3]);
-    }
-    __device__ static uint4 pack(const float (&acc)[4]) {
-        return make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]), __float_as_uint(acc[2]),
-                          __float_as_uint(acc[3]));
-    }
-};
-
-template <int kBf16>
 __global__ void __launch_bounds__(kCombThreads)
 combine_kernel(const uint4 *__restrict__ y, const int32_t *__restrict__ pos,
                const float *__restrict__ topk_w, int64_t NT, int R, int nvec, int64_t row_lo,
                int64_t row_hi, uint4 *__restrict__ out) {
-    using VT = VecTraits<kBf16>;
+    using VT = Vec<kBf16>;
     constexpr int EL = VT::kElems;
     __shared__ int s_pos[32];
     __shared__ float s_w[32];

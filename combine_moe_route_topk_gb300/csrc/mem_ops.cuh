@@ -57,4 +57,24 @@ __device__ __forceinline__ void prefetch_rows_l2(const void *base, int64_t row_b
     }
 }
 
+// Division of 32-bit dividends below 2^31 by a divisor fixed for a launch
+// (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994): with l = ceil(log2 d) and m = floor(2^32 (2^l - d)
+// / d) + 1, n / d = (umulhi(n, m) + n) >> l.  The host computes (m, l) once;
+// the kernel spends a multiply-high, an add and a shift per division.
+struct FastDiv {
+    uint32_t mul, shift;
+};
+
+inline FastDiv make_fast_div(uint32_t d) {  // d >= 1
+    uint32_t l = 0;
+    while (l < 32 && (1ull << l) < d) ++l;
+    const uint64_t m = (((1ull << 32) * ((1ull << l) - d)) / d) + 1;
+    return FastDiv{(uint32_t)m, l};
+}
+
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, FastDiv f) {
+    return (__umulhi(n, f.mul) + n) >> f.shift;
+}
+
 }  // namespace moe

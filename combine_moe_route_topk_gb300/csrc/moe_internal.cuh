@@ -71,6 +71,15 @@ cudaError_t launch_combine(const void *y, int y_dtype, const int32_t *pos, const
                            int64_t NT, int R, int H, int64_t row_lo, int64_t row_hi, void *out,
                            cudaStream_t stream);
 
+// Expert-parallel local path of one rank (rows [row_lo, row_hi) only).
+cudaError_t launch_pack_rank(const void *x, const float *x_scales, const int32_t *pos, int64_t NT,
+                             int R, int64_t row_bytes, int scales_per_row, int64_t row_lo,
+                             int64_t row_hi, void *packed_x, float *packed_scales,
+                             int32_t *packed_src, cudaStream_t stream);
+cudaError_t launch_combine_rank(const void *y, int y_dtype, const int32_t *pos, const float *topk_w,
+                                int64_t NT, int R, int H, int64_t row_lo, int64_t row_hi, void *out,
+                                cudaStream_t stream);
+
 cudaError_t launch_combine_partials(const void *y, int y_dtype, const int32_t *pos,
                                     const float *topk_w, int64_t NT, int R, int H, int64_t cap,
                                     int64_t rows_total, int P, void *partial, int32_t *slot_rank,

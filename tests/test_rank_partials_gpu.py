@@ -31,6 +31,14 @@ CASES = {
     "tiny": W.WORKLOADS["tiny"],
     "r16_f32": W.Workload("r16_f32", N=4, T=100, E=64, R=16, H=64, x_dtype=W.F32,
                           y_dtype=W.F32, expert_op=W.EXPERT_SCALE, seed=51),
+    # row widths that are not powers of two (66 and 25 vectors) and a
+    # token count that is not a multiple of the 8 tokens of a rank-local block
+    "odd_f32": W.Workload("odd_f32", N=3, T=333, E=48, R=6, H=264, x_dtype=W.F32,
+                          y_dtype=W.F32, seed=52),
+    "odd_bf16": W.Workload("odd_bf16", N=5, T=77, E=40, R=3, H=200, seed=53),
+    # fp8 rows with block scales through the rank-restricted pack
+    "fp8": W.Workload("fp8", N=4, T=50, E=32, R=4, H=384, x_dtype=W.FP8E4M3_BLK128,
+                      expert_op=W.EXPERT_DEQUANT, seed=54),
 }
 
 
@@ -46,7 +54,7 @@ def _setup(w):
     return inp, gr, ref
 
 
-@pytest.mark.parametrize("name", ["tiny", "qwen_small"])
+@pytest.mark.parametrize("name", ["tiny", "qwen_small", "odd_f32", "odd_bf16", "fp8"])
 def test_pack_rank_writes_only_that_region(name):
     w = CASES[name]
     inp = W.make_inputs(w)
@@ -65,6 +73,8 @@ def test_pack_rank_writes_only_that_region(name):
     rt = torch.from_numpy(rows).to(b.packed_x.device)
     np.testing.assert_array_equal(oracle.x_as_bytes(b.packed_x[rt].cpu()), ref["packed_x"][crow])
     np.testing.assert_array_equal(b.packed_src[rt].cpu().numpy(), ref["packed_src"][crow])
+    if b.packed_scales is not None:
+        np.testing.assert_array_equal(b.packed_scales[rt].cpu().numpy(), ref["packed_scales"][crow])
     others = torch.ones(b.packed_src.numel(), dtype=torch.bool, device=rt.device)
     others[rt] = False
     assert bool((b.packed_src[others] == -7).all())
