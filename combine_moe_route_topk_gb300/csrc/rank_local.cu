@@ -25,7 +25,7 @@ namespace {
 
 constexpr int kLThreads = 256;
 constexpr int kLTok = 8;   // tokens per block (one lane of warp 0 each)
-constexpr int kLU = 4;     // vectors per thread in flight (pack)
+constexpr int kLU = 8;     // vectors per thread in flight (pack)
 constexpr int kLCU = 4;    // output vectors per thread in flight (combine)
 constexpr int kLKB = 2;    // rows of one token loaded together (combine)
 constexpr int kLPB = 8;    // positions of one token loaded together
@@ -123,6 +123,8 @@ combine_rank_kernel(const uint4 *__restrict__ y, const int32_t *__restrict__ pos
     __shared__ int s_p[kLTok][32];  // per token: its pairs in the region, in k order
     __shared__ float s_w[kLTok][32];
     __shared__ int s_cnt[kLTok];
+    __shared__ int s_tok[kLTok];    // tokens with pairs first, then the others
+    __shared__ int s_nnz;
     const int tid = threadIdx.x, lane = tid & 31;
     const int64_t g0 = (int64_t)blockIdx.x * kLTok;
     grid_dependency_wait();  // y, pos and topk_w come from earlier kernels
@@ -137,10 +139,22 @@ combine_rank_kernel(const uint4 *__restrict__ y, const int32_t *__restrict__ pos
                 ++cnt;
             });
         s_cnt[lane] = cnt;
+        const unsigned nz = __ballot_sync((1u << kLTok) - 1u, cnt > 0 && g < NT);
+        const unsigned z = __ballot_sync((1u << kLTok) - 1u, cnt == 0 && g < NT);
+        const unsigned below = (1u << lane) - 1u;
+        if (g < NT) s_tok[cnt > 0 ? __popc(nz & below) : __popc(nz) + __popc(z & below)] = lane;
+        if (lane == 0) s_nnz = __popc(nz);
     }
     __syncthreads();
     const int ntok = (int)((NT - g0) < kLTok ? (NT - g0) : kLTok);
-    const int total = ntok * nvec;  // < 2^31: checked by the launcher
+    const int nnz = s_nnz;
+    // tokens without a pair on the rank: zero rows, plain stores
+    for (int zt = nnz; zt < ntok; ++zt) {
+        uint4 *row = out + (g0 + s_tok[zt]) * nvec;
+        for (int c = tid; c < nvec; c += kLThreads) row[c] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    // tokens with pairs: flattened (token, vector) work
+    const int total = nnz * nvec;  // < 2^31: checked by the launcher
     for (int i0 = tid; i0 < total; i0 += kLThreads * kLCU) {
         int t[kLCU], c[kLCU], n[kLCU];
         float acc[kLCU][EL];
@@ -152,8 +166,9 @@ combine_rank_kernel(const uint4 *__restrict__ y, const int32_t *__restrict__ pos
             c[u] = 0;
             n[u] = 0;
             if (i < total) {
-                t[u] = (int)fast_div((uint32_t)i, div_nvec);
-                c[u] = i - t[u] * nvec;
+                const int q = (int)fast_div((uint32_t)i, div_nvec);
+                t[u] = s_tok[q];
+                c[u] = i - q * nvec;
                 n[u] = s_cnt[t[u]];
             }
             nmax = n[u] > nmax ? n[u] : nmax;
