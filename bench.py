@@ -184,10 +184,11 @@ class ClockSampler:
 # CPU oracle timing (baseline / reference arm)
 # --------------------------------------------------------------------------
 
-def oracle_pass(w, inp, tokens=None):
+def oracle_pass(w, inp, tokens=None, phases=None):
     """One oracle pass of route -> count -> pack -> combine (identity expert)
     over the whole batch, or over the first `tokens` tokens treated as a
-    smaller batch of the same shape (T' = tokens / N per rank)."""
+    smaller batch of the same shape (T' = tokens / N per rank).  With a
+    `phases` dict, the seconds of each step are added to it."""
     import numpy as np
     import oracle
     logits, bias = inp.logits.numpy(), None if inp.bias is None else inp.bias.numpy()
@@ -196,25 +197,34 @@ def oracle_pass(w, inp, tokens=None):
     if tokens is not None:
         T = max(1, tokens // w.N)
         logits, xb = logits[:w.N * T], xb[:w.N * T]
+    t = [time.perf_counter()]
     idx, tw, _ = oracle.route(logits, bias, w.R, w.score_fn, w.renormalize)
+    t.append(time.perf_counter())
     cap = w.N * T * max(w.R, w.E // w.N)
     cnt, _ = oracle.count(w.N, T, w.E, cap, idx)
+    t.append(time.perf_counter())
     px, _, _ = oracle.pack(xb, None, cnt["pos"], cnt["rank_offsets"], cap)
+    t.append(time.perf_counter())
     y = px.view(np.uint16) if w.y_dtype == 0 else px.view(np.float32)
     oracle.combine(y, w.y_dtype, cnt["pos"], cnt["rank_offsets"], tw, cap, w.H)
+    t.append(time.perf_counter())
+    if phases is not None:
+        for k, a, b in zip(KERNELS, t, t[1:]):
+            phases[k] = phases.get(k, 0.0) + (b - a)
     return w.N * T
 
 
 def cpu_baseline(w, inp, seconds):
-    n_tok, passes = 0, 0
+    n_tok, passes, phases = 0, 0, {}
     t0 = time.perf_counter()
     while True:
-        n_tok += oracle_pass(w, inp)
+        n_tok += oracle_pass(w, inp, phases=phases)
         passes += 1
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
     return {"value": n_tok / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "phase_ms_per_pass": {k: v / passes * 1e3 for k, v in phases.items()},
             "sample": f"{passes} full pass(es) of the {w.name} batch ({w.NT} tokens): "
                       f"route, count, pack, combine; single-threaded C, {dt:.1f} s"}
 
