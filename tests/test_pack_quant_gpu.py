@@ -71,8 +71,10 @@ def test_quant_pack_full_size_kimi():
     _run(w, W.make_inputs(w))
 
 
+# the last shape has 72 KB rows: 2304 chunks per row, more than one pass of a
+# 1024-thread block, and too wide for the L2 prefetch of x
 @pytest.mark.parametrize("N,T,E,R,H", [(3, 77, 24, 3, 128), (4, 50, 32, 5, 384),
-                                       (2, 300, 16, 2, 1152)])
+                                       (2, 300, 16, 2, 1152), (2, 24, 8, 3, 36864)])
 def test_quant_pack_ragged(N, T, E, R, H):
     w = W.Workload("q", N=N, T=T, E=E, R=R, H=H, seed=N * T)
     _run(w, W.make_inputs(w))

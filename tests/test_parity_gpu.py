@@ -113,6 +113,10 @@ REDUCED = {
                              seed=9),
     # R > 8 uses the 512-thread count kernel
     "r16": W.Workload("r16", N=4, T=600, E=64, R=16, H=64, score_fn=W.SIGMOID, seed=10),
+    # 72 KB bf16 rows: pack and combine run several passes of a 1024-thread
+    # block per row, and pack skips its L2 prefetch (rows over 64 KB)
+    "wide_rows": W.Workload("wide_rows", N=2, T=24, E=8, R=3, H=36864, renormalize=True,
+                            expert_op=W.EXPERT_SCALE, seed=16),
     # bf16 rows, f32 expert outputs
     "bf16_to_f32": W.Workload("bf16_to_f32", N=2, T=64, E=16, R=2, H=512, y_dtype=W.F32,
                               seed=11),
