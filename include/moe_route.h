@@ -25,6 +25,13 @@
  *   - Device-side problems (a rank over capacity, invalid expert ids) never
  *     trap: moe_dispatch_count writes a status word on the device, pos
  *     entries of affected pairs become -1, and later steps skip them.
+ *   - Kernels are launched with programmatic stream serialization and let
+ *     the next kernel in the stream be scheduled early (before their own
+ *     results are complete).  This only matters to a caller whose own next
+ *     kernel is also launched with that attribute: such a kernel must wait
+ *     (griddepcontrol.wait / cudaGridDependencySynchronize) before it reads
+ *     anything the library writes.  Kernels launched without it, copies and
+ *     events are ordered as usual.
  */
 #ifndef MOE_ROUTE_H
 #define MOE_ROUTE_H
