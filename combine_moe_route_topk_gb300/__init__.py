@@ -98,6 +98,7 @@ def lib() -> ctypes.CDLL:
             L.moe_combine_reduce_partials.argtypes = [D, P, P, P, P]
             L.moe_read_status.argtypes = [P, P]
             L.moe_take_device_error.argtypes = [P]
+            L.moe_selftest_bounded_wait.argtypes = [P, ctypes.c_int64, P]
             L.moe_last_error.restype = ctypes.c_char_p
             L.moe_last_error.argtypes = []
             L.moe_version.restype = i32
@@ -106,7 +107,7 @@ def lib() -> ctypes.CDLL:
                        "moe_dispatch_fused", "moe_dispatch_fused_static",
                        "moe_combine", "moe_combine_rank", "moe_combine_partials",
                        "moe_combine_reduce_partials", "moe_read_status",
-                       "moe_take_device_error"):
+                       "moe_take_device_error", "moe_selftest_bounded_wait"):
                 getattr(L, fn).restype = i32
             _lib = L
     return _lib
@@ -351,6 +352,13 @@ def take_device_error(stream=None) -> int:
     if rc == MOE_ERR_CUDA:
         raise MoeError(rc, lib().moe_last_error().decode())
     return rc
+
+
+def selftest_bounded_wait(status, polls: int, stream=None) -> None:
+    """Enqueue the bounded-wait self-test: status[0] becomes MOE_OK if
+    status[1] turned nonzero within `polls` polls, else MOE_ERR_TIMEOUT."""
+    _check(lib().moe_selftest_bounded_wait(_ptr(status, 8, "status", torch.int32), int(polls),
+                                           _stream(stream)))
 
 
 class Buffers:

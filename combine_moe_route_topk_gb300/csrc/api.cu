@@ -420,6 +420,17 @@ int moe_dispatch_fused_static(const MoeDims *dims, const float *logits, const fl
                               status, packed_x, packed_scales, packed_src, scratch, stream);
 }
 
+int moe_selftest_bounded_wait(int32_t *status, int64_t polls, void *stream) {
+    g_err[0] = '\0';
+    if (!status || !aligned(status, 4))
+        return set_error(MOE_ERR_INVALID_ARG, "moe_selftest_bounded_wait: status must be a 4-byte aligned pointer");
+    if (polls < 1 || polls > ((int64_t)1 << 20))
+        return set_error(MOE_ERR_INVALID_ARG, "moe_selftest_bounded_wait: polls %lld outside [1, 2^20]",
+                         (long long)polls);
+    return cuda_result(launch_selftest_wait(status, (long long)polls, (cudaStream_t)stream),
+                       "moe_selftest_bounded_wait");
+}
+
 int moe_take_device_error(void *stream) {
     g_err[0] = '\0';
     int err = 0;

@@ -74,6 +74,19 @@ __device__ __forceinline__ int ld_acquire(const int *p) {
 
 // Barrier of `nblocks` blocks on (arrive, gen) words of the workspace.
 // Returns false when the wait gave up or another block recorded an error.
+// Polls *word until it differs from `value`, at most `limit` times with a
+// growing sleep between polls (32 ns doubling to 512 ns); false if it gave up.
+__device__ bool wait_while_equal(const int *word, int value, long long limit) {
+    long long it = 0;
+    unsigned ns = 32;
+    while (ld_acquire(word) == value) {
+        if (++it > limit) return false;
+        __nanosleep(ns);
+        if (ns < 512) ns <<= 1;  // back off: hundreds of blocks poll one word
+    }
+    return true;
+}
+
 __device__ bool bounded_barrier(int *arrive, int *gen, int nblocks, int *err) {
     __shared__ int s_ok;
     __syncthreads();
@@ -85,18 +98,9 @@ __device__ bool bounded_barrier(int *arrive, int *gen, int nblocks, int *err) {
             atomicExch(arrive, 0);
             __threadfence();
             atomicAdd(gen, 1);  // release the others
-        } else {
-            long long it = 0;
-            unsigned ns = 32;
-            while (ld_acquire(gen) == g0) {
-                if (++it > kSpinLimit) {
-                    atomicCAS(err, 0, MOE_ERR_TIMEOUT);
-                    ok = 0;
-                    break;
-                }
-                __nanosleep(ns);
-                if (ns < 512) ns <<= 1;  // back off: hundreds of blocks poll one word
-            }
+        } else if (!wait_while_equal(gen, g0, kSpinLimit)) {
+            atomicCAS(err, 0, MOE_ERR_TIMEOUT);
+            ok = 0;
         }
         __threadfence();
         s_ok = ok && ld_acquire(err) == 0;
@@ -543,6 +547,28 @@ cudaError_t launch_dispatch_fused(const float *logits, const float *bias, int sc
     return launch_fused_j<16>(P, stream);
 }
 
+}  // namespace moe
+
+// ---- self-test of the bounded wait -----------------------------------------
+//
+// One thread waits, through the same bounded poll as the grid barriers, for
+// status[1] to become nonzero; status[0] gets MOE_OK if it did and
+// MOE_ERR_TIMEOUT if the wait gave up.  Nothing in the library writes
+// status[1], so unless the caller set it beforehand the wait runs out: this
+// shows on a given GPU that a wait which is never satisfied ends with a
+// status the host can read, and leaves the context usable.
+namespace moe {
+namespace {
+__global__ void selftest_wait_kernel(int *status, long long polls) {
+    if (threadIdx.x == 0 && blockIdx.x == 0)
+        status[0] = wait_while_equal(status + 1, 0, polls) ? MOE_OK : MOE_ERR_TIMEOUT;
+}
+}  // namespace
+
+cudaError_t launch_selftest_wait(int32_t *status, long long polls, cudaStream_t stream) {
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(status, polls);
+    return cudaGetLastError();
+}
 }  // namespace moe
 
 // ---- allocation-free variant -------------------------------------------------

@@ -57,6 +57,10 @@ cudaError_t launch_dispatch_fused(const float *logits, const float *bias, int sc
                                   int32_t *pos, int32_t *status, void *packed_x, float *packed_scales,
                                   int32_t *packed_src, void *workspace, cudaStream_t stream);
 
+// Bounded-wait self-test: status[0] <- MOE_OK / MOE_ERR_TIMEOUT after waiting
+// (at most `polls` polls) for status[1] to become nonzero.
+cudaError_t launch_selftest_wait(int32_t *status, long long polls, cudaStream_t stream);
+
 // Scratch for the allocation-free fused dispatch: a fixed device array of
 // the library (size in bytes; address on the current device).
 int64_t fused_static_scratch_bytes();

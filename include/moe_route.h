@@ -307,6 +307,21 @@ int moe_combine_reduce_partials(const MoeDims *dims, const void *partial, const 
  * MOE_ERR_CUDA if the wait or the copy failed. */
 int moe_read_status(const int32_t *status, void *stream);
 
+/* Self-test of the library's bounded waits (the pages have no counterpart:
+ * this is a diagnostic of this implementation).  Enqueues one thread that
+ * waits, with the same bounded poll the decode-fused kernel uses at its
+ * grid barriers (a sleep of 32 ns doubling to 512 ns between polls), for
+ * status[1] to become nonzero, at most `polls` times (1 <= polls <= 2^20,
+ * about half a second at the upper end).  status[0] then becomes MOE_OK if
+ * the word changed and MOE_ERR_TIMEOUT if the wait gave up.  Nothing in the
+ * library writes status[1]: left at zero, the wait runs out, which shows
+ * that a wait that is never satisfied ends with a status the host can read
+ * and leaves the context usable.
+ *   status  i32 [2] (device; [1] is read, [0] written)
+ * Returns MOE_OK once enqueued (read status[0] after synchronising),
+ * MOE_ERR_INVALID_ARG or MOE_ERR_CUDA. */
+int moe_selftest_bounded_wait(int32_t *status, int64_t polls, void *stream);
+
 /* Wait for `stream`, then return and clear the library's device error word:
  * MOE_OK, or MOE_ERR_TIMEOUT if a bounded wait inside one of the library's
  * kernels gave up since the last call (that kernel's output is then
