@@ -552,7 +552,8 @@ def run_ours(args):
         fm = statistics.mean(a.elapsed_time(c) for a, c in fe)
         fused = {"ms": fm, "vs_separate_dispatch_ms": per_timed["dispatch (route+count+pack)"],
                  "step_ms_if_used": fm + per_timed["combine"],
-                 "note": "moe_dispatch_fused (one cooperative launch) on the same batch"}
+                 "note": "moe_dispatch_fused on the same batch (one thread-block cluster for "
+                         "batches of up to 512 tokens, else one cooperative launch)"}
         del ws
     except moe.MoeError as ex:
         fused = {"unsupported": str(ex)}

@@ -510,6 +510,16 @@ cudaError_t launch_dispatch_fused(const float *logits, const float *bias, int sc
                                   int32_t *rank_counts, int32_t *rank_offsets, int32_t *send_counts,
                                   int32_t *pos, int32_t *status, void *packed_x, float *packed_scales,
                                   int32_t *packed_src, void *workspace, cudaStream_t stream) {
+    // Small batches: one thread-block cluster, no grid barriers and no
+    // workspace (the cooperative kernel below handles everything else, and
+    // takes over if the device cannot schedule the cluster).
+    if (dispatch_small_eligible((int64_t)N * T, E, R, row_bytes)) {
+        cudaError_t e = launch_dispatch_small(logits, bias, score_fn, renormalize, x, x_scales, N, T, E, R,
+                                              row_bytes, spr, cap, topk_idx, topk_w, expert_counts,
+                                              expert_offsets, rank_counts, rank_offsets, send_counts, pos,
+                                              status, packed_x, packed_scales, packed_src, stream);
+        if (e != cudaErrorNotSupported) return e;
+    }
     FusedParams P;
     P.logits = logits;
     P.bias = bias;
@@ -541,6 +551,10 @@ cudaError_t launch_dispatch_fused(const float *logits, const float *bias, int sc
     P.packed_src = packed_src;
     P.ws = reinterpret_cast<int *>(workspace);
     const int need = (E + 31) / 32;
+    // the same experts per lane as the route kernel, so that the softmax
+    // denominator is summed in the same order and the weights agree bit for bit
+    if (need <= 1) return launch_fused_j<1>(P, stream);
+    if (need <= 2) return launch_fused_j<2>(P, stream);
     if (need <= 4) return launch_fused_j<4>(P, stream);
     if (need <= 8) return launch_fused_j<8>(P, stream);
     if (need <= 12) return launch_fused_j<12>(P, stream);

@@ -57,6 +57,16 @@ cudaError_t launch_dispatch_fused(const float *logits, const float *bias, int sc
                                   int32_t *pos, int32_t *status, void *packed_x, float *packed_scales,
                                   int32_t *packed_src, void *workspace, cudaStream_t stream);
 
+// Small decode batches: route + count + pack in one thread-block cluster.
+bool dispatch_small_eligible(int64_t NT, int E, int R, int64_t row_bytes);
+cudaError_t launch_dispatch_small(const float *logits, const float *bias, int score_fn, int renormalize,
+                                  const void *x, const float *x_scales, int N, int T, int E, int R,
+                                  int64_t row_bytes, int spr, int64_t cap, int32_t *topk_idx,
+                                  float *topk_w, int32_t *expert_counts, int32_t *expert_offsets,
+                                  int32_t *rank_counts, int32_t *rank_offsets, int32_t *send_counts,
+                                  int32_t *pos, int32_t *status, void *packed_x, float *packed_scales,
+                                  int32_t *packed_src, cudaStream_t stream);
+
 // Bounded-wait self-test: status[0] <- MOE_OK / MOE_ERR_TIMEOUT after waiting
 // (at most `polls` polls) for status[1] to become nonzero.
 cudaError_t launch_selftest_wait(int32_t *status, long long polls, cudaStream_t stream);

@@ -50,9 +50,10 @@ __device__ __forceinline__ void sort_desc(uint32_t (&k)[JP], int (&sl)[JP]) {
     }
 }
 
-// Route token g with the calling warp (all 32 lanes).
+// Route token g with the calling warp (all 32 lanes).  Returns, in lane
+// k < R, the expert of pair k (what it writes to topk_idx[g][k]).
 template <int J, bool kVec4>
-__device__ __forceinline__ void route_token(const float *__restrict__ logits,
+__device__ __forceinline__ int route_token(const float *__restrict__ logits,
                                             const float *__restrict__ bias, int64_t g, int E, int R,
                                             int score_fn, int renormalize,
                                             int32_t *__restrict__ topk_idx,
@@ -193,6 +194,7 @@ __device__ __forceinline__ void route_token(const float *__restrict__ logits,
         topk_idx[g * R + lane] = my_e;
         topk_w[g * R + lane] = p;
     }
+    return my_e;
 }
 
 }  // namespace route_impl
