@@ -24,8 +24,8 @@
 //   pack     the block copies its own tokens' rows to their positions.
 // Counts, offsets and send counts are integer sums, so every output equals
 // that of the separate route, count and pack kernels bit for bit.
-// Used for N*T <= 512 tokens (16 blocks of 32), E <= 256 and a pack of at
-// most 16 MB (more rows would be copied by too few SMs).
+// Used for N*T <= 512 tokens (16 blocks of 32), E <= 256 and at most 1 MB of
+// rows read and written per block (more would be copied by too few SMs).
 #include <cooperative_groups.h>
 
 #include "mem_ops.cuh"
@@ -43,7 +43,12 @@ constexpr int kSTok = 32;        // tokens per block
 constexpr int kSMaxBlocks = 16;  // non-portable cluster size limit
 constexpr int kSPackU = 4;       // row vectors per thread in flight while packing
 constexpr int kSMaxE = 256;  // 8 experts per lane: the route body fits 64 registers
-constexpr int64_t kSMaxPackBytes = 16ll << 20;  // beyond this, too few SMs copy the rows
+// Rows read and written per block (32 tokens x (1 + R) rows).  The pack
+// runs on at most 16 SMs; up to about this much per block it still beats
+// the cooperative kernel (measured on GB300, cluster vs cooperative: 300 KB
+// per block 21 vs 35 us, 880 KB 27 vs 34 us, 1.2 MB 33 vs 32 us, 4 MB 74 vs
+// 40 us).  The three separate calls beat both beyond about 200 KB per block.
+constexpr int64_t kSMaxBlockPackBytes = 1 << 20;
 
 struct SmallParams {
     const float *logits;
@@ -288,8 +293,9 @@ cudaError_t launch_small_j(const SmallParams &P, int C, cudaStream_t stream) {
 }  // namespace
 
 bool dispatch_small_eligible(int64_t NT, int E, int R, int64_t row_bytes) {
+    const int64_t per_block = NT < kSTok ? NT : kSTok;
     return NT >= 1 && NT <= (int64_t)kSTok * kSMaxBlocks && E <= kSMaxE && R <= 32 &&
-           NT * (R + 1) * row_bytes <= kSMaxPackBytes;
+           per_block * (R + 1) * row_bytes <= kSMaxBlockPackBytes;
 }
 
 cudaError_t launch_dispatch_small(const float *logits, const float *bias, int score_fn, int renormalize,

@@ -42,9 +42,13 @@ CASES = {
     "e512": W.Workload("e512", N=16, T=64, E=512, R=8, H=128, renormalize=True, seed=64),
     # capacity overflow reported through the status word
     "capacity": W.Workload("capacity", N=4, T=64, E=16, R=2, H=128, cap_rows=100, seed=65),
-    # the largest batch the single-cluster path takes: 16 blocks of 32 tokens, E = 256
-    "small_max": W.Workload("small_max", N=16, T=32, E=256, R=8, H=1024, score_fn=W.SIGMOID,
+    # the largest batch the single-cluster path takes: 16 blocks of 32 tokens,
+    # E = 256, R = 8 (rows of 512 bytes: 147 KB read and written per block)
+    "small_max": W.Workload("small_max", N=16, T=32, E=256, R=8, H=256, score_fn=W.SIGMOID,
                             renormalize=True, bias="normal", seed=66),
+    # past the cluster path's per-block row traffic (1.2 MB): cooperative kernel
+    "past_small": W.Workload("past_small", N=16, T=32, E=256, R=8, H=2048, score_fn=W.SIGMOID,
+                             renormalize=True, bias="normal", seed=67),
 }
 
 
@@ -56,9 +60,10 @@ def test_fused_cases(name):
     assert gr.status == (oracle.ERR_CAPACITY if name == "capacity" else oracle.OK)
 
 
-# dsv3_decode takes the cooperative kernel; tiny and small_max the single
-# thread-block cluster (up to 512 tokens, E <= 256, a pack of at most 16 MB)
-@pytest.mark.parametrize("name", ["dsv3_decode", "tiny", "small_max"])
+# dsv3_decode and past_small take the cooperative kernel; tiny and small_max
+# the single thread-block cluster (up to 512 tokens, E <= 256, at most 1 MB of
+# rows read and written per 32 tokens)
+@pytest.mark.parametrize("name", ["dsv3_decode", "past_small", "tiny", "small_max"])
 def test_fused_equals_separate_calls_bytewise(name):
     w = W.WORKLOADS.get(name) or CASES[name]
     inp = W.make_inputs(w)
