@@ -90,19 +90,29 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+# headers that only declare host functions: of these, only the macro
+# definitions (status codes, dtypes, flags) can change a kernel
+DECLARATION_HEADERS = ("moe_internal.cuh", "moe_route.h")
+
+
 def source_hash(name: str) -> str:
-    """Hash of a kernel source file and every local header it includes."""
-    csrc = os.path.join(ROOT, "combine_moe_route_topk_gb300", "csrc")
+    """Hash of a kernel source file and every local header it includes (the
+    declaration headers through their #define lines only)."""
+    dirs = [os.path.join(ROOT, "combine_moe_route_topk_gb300", "csrc"), os.path.join(ROOT, "include")]
     h = hashlib.sha256()
     todo, seen = [name], set()
     while todo:
         f = todo.pop(0)
-        if f in seen or not os.path.exists(os.path.join(csrc, f)):
+        path = next((os.path.join(d, f) for d in dirs if os.path.exists(os.path.join(d, f))), None)
+        if f in seen or path is None:
             continue
         seen.add(f)
-        with open(os.path.join(csrc, f), "rb") as fh:
+        with open(path, "rb") as fh:
             data = fh.read()
-        h.update(f.encode() + b"\0" + data)
+        part = data
+        if f in DECLARATION_HEADERS:
+            part = b"\n".join(l for l in data.splitlines() if l.lstrip().startswith(b"#define"))
+        h.update(f.encode() + b"\0" + part)
         todo += [m.decode() for m in re.findall(rb'#include "([^"]+)"', data)]
     return h.hexdigest()[:16]
 
