@@ -46,6 +46,8 @@ CASES = {
     # E = 256, R = 8 (rows of 512 bytes: 147 KB read and written per block)
     "small_max": W.Workload("small_max", N=16, T=32, E=256, R=8, H=256, score_fn=W.SIGMOID,
                             renormalize=True, bias="normal", seed=66),
+    # a cluster of one block: one rank, 32 tokens
+    "one_block": W.Workload("one_block", N=1, T=32, E=8, R=2, H=64, bias="normal", seed=68),
     # past the cluster path's per-block row traffic (1.2 MB): cooperative kernel
     "past_small": W.Workload("past_small", N=16, T=32, E=256, R=8, H=2048, score_fn=W.SIGMOID,
                              renormalize=True, bias="normal", seed=67),
