@@ -382,7 +382,9 @@ def run_ours(args):
         # events, and Python needs tens of microseconds per call: a GPU sleep
         # long enough for the host to enqueue the whole loop first keeps that
         # host time out of every interval.
-        torch.cuda._sleep(int(iters * 150e-6 * 2.0e9))
+        sleep = getattr(torch.cuda, "_sleep", None)  # a private helper of torch
+        if sleep is not None:
+            sleep(int(iters * 150e-6 * 2.0e9))
 
     for _ in range(max(3, args.warmup)):
         flush()
