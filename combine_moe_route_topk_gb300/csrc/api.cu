@@ -83,6 +83,8 @@ int check_dims(const MoeDims *d, Derived *out, const char *what) {
                          d->y_dtype);
     if (d->H % 8 != 0)
         return set_error(MOE_ERR_INVALID_ARG, "%s: H=%d must be a multiple of 8", what, d->H);
+    if (d->H > (1 << 24))  // keeps per-row vector counts and in-row indices in 32 bits
+        return set_error(MOE_ERR_UNSUPPORTED, "%s: this build supports H <= 2^24 (got H=%d)", what, d->H);
     if (d->x_dtype == MOE_FP8E4M3_BLK128 && d->H % 128 != 0)
         return set_error(MOE_ERR_INVALID_ARG, "%s: fp8 rows need H %% 128 == 0 (got H=%d)", what, d->H);
     if (d->cap_rows < 0) return set_error(MOE_ERR_INVALID_ARG, "%s: cap_rows < 0", what);

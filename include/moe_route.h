@@ -71,7 +71,8 @@ typedef struct MoeDims {
     int32_t T;        /* tokens per rank */
     int32_t E;        /* experts; expert e lives on rank e / (E/N) */
     int32_t R;        /* experts per token */
-    int32_t H;        /* hidden size (elements per token row) */
+    int32_t H;        /* hidden size (elements per token row); H % 8 == 0,
+                         H % 128 == 0 for fp8 rows, H <= 2^24 */
     int32_t x_dtype;  /* MOE_BF16, MOE_F32 or MOE_FP8E4M3_BLK128: dispatched rows */
     int32_t y_dtype;  /* MOE_BF16 or MOE_F32: expert outputs read by combine and its output */
     int32_t reserved; /* must be 0 */

@@ -129,6 +129,13 @@ def test_fused_dispatch_rejects_non_decode_shapes(lib):
         assert why in lib.moe_last_error().decode()
 
 
+def test_rows_wider_than_2_24_elements_are_unsupported(lib):
+    d = moe.make_dims(2, 8, 4, 2, (1 << 24) + 8)
+    s = moe.MoeSizes()
+    assert lib.moe_buffer_sizes(ctypes.byref(d), ctypes.byref(s)) == moe.MOE_ERR_UNSUPPORTED
+    assert "2^24" in lib.moe_last_error().decode()
+
+
 def test_reserved_field_must_be_zero(lib):
     d = moe.make_dims(4, 8, 16, 2, 64)
     d.reserved = 1
