@@ -64,8 +64,8 @@ extern "C" {
 #define MOE_BIAS_SELECT_ONLY 0x10
 
 /* Problem dimensions.  Limits: N >= 1, T >= 0, 1 <= E <= 1024, E % N == 0,
- * 1 <= R <= min(E, 32), H >= 8 and H % 8 == 0 (H % 128 == 0 for fp8 x),
- * N*T*R < 2^31, N*cap_rows < 2^31. */
+ * 1 <= R <= min(E, 32), 8 <= H <= 2^24 and H % 8 == 0 (H % 128 == 0 for
+ * fp8 x), N*T*R < 2^31, N*cap_rows < 2^31. */
 typedef struct MoeDims {
     int32_t N;        /* ranks (partitions of one GPU's memory) */
     int32_t T;        /* tokens per rank */
