@@ -56,18 +56,25 @@ __host__ __device__ inline int count_ksub(int threads, int E) {
 
 // kWarps 32-token groups per tile (one token per thread); kSub parts of the
 // group prefix per expert.
+// Every section starts on a 16-byte boundary (fin is read as int2, and E
+// may be odd).
 __host__ __device__ inline CountSmem count_smem_layout(int E, int kWarps, int kSub) {
     CountSmem s;
     int o = 0;
-    s.gmask = o;  o += kWarps * E * 4;     // u32 [kWarps][E]: group masks, then group prefixes
-    s.subsum = o; o += kSub * E * 4;       // group-prefix partial sums
-    s.run = o;    o += 2 * E * 4;          // pairs of this block so far (double buffered)
-    s.base = o;   o += E * 4;              // pairs in earlier blocks
-    s.tot = o;    o += E * 4;              // pairs in all blocks
-    s.eoff = o;   o += (E + 1) * 4 + 12;   // exclusive scan of tot (+ pad to 16 B)
-    s.fin = o;    o += E * 8;              // int2 per expert: first row, rows left before cap
-    s.send = o;   o += kSendSmem * 4;      // this block's send counts, rows s_first..
-    s.flags = o;  o += 64 + 32 * 4;        // [0]: invalid pair seen; [16..48): scan partials
+    auto take = [&o](int bytes) {
+        const int at = o;
+        o += (bytes + 15) & ~15;
+        return at;
+    };
+    s.gmask = take(kWarps * E * 4);   // u32 [kWarps][E]: group masks, then group prefixes
+    s.subsum = take(kSub * E * 4);    // group-prefix partial sums
+    s.run = take(2 * E * 4);          // pairs of this block so far (double buffered)
+    s.base = take(E * 4);             // pairs in earlier blocks
+    s.tot = take(E * 4);              // pairs in all blocks
+    s.eoff = take((E + 1) * 4);       // exclusive scan of tot
+    s.fin = take(E * 8);              // int2 per expert: first row, rows left before cap
+    s.send = take(kSendSmem * 4);     // this block's send counts, rows s_first..
+    s.flags = take(64 + 32 * 4);      // [0]: invalid pair seen; [16..48): scan partials
     s.bytes = o;
     return s;
 }

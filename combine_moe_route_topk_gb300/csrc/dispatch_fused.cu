@@ -127,17 +127,23 @@ struct FusedSmem {
     int gmask, run, base, tot, eoff, fin, send, misc, bytes;
 };
 
+// Every section starts on a 16-byte boundary (fin is read as int2).
 __host__ __device__ inline FusedSmem fused_smem_layout(int E) {
     FusedSmem s;
     int o = 0;
-    s.gmask = o; o += kFWarps * E * 4;   // group masks, then group prefixes
-    s.run = o;   o += E * 4;             // this block's histogram
-    s.base = o;  o += E * 4;             // pairs in earlier count blocks
-    s.tot = o;   o += E * 4;             // pairs in all count blocks
-    s.eoff = o;  o += (E + 1) * 4 + 12;  // exclusive scan of tot
-    s.fin = o;   o += E * 8;             // first row / rows left per expert
-    s.send = o;  o += kSendStage * 4;    // send counts of this block's source ranks
-    s.misc = o;  o += 64 * 4;            // flags and scan partials
+    auto take = [&o](int bytes) {
+        const int at = o;
+        o += (bytes + 15) & ~15;
+        return at;
+    };
+    s.gmask = take(kFWarps * E * 4);  // group masks, then group prefixes
+    s.run = take(E * 4);              // this block's histogram
+    s.base = take(E * 4);             // pairs in earlier count blocks
+    s.tot = take(E * 4);              // pairs in all count blocks
+    s.eoff = take((E + 1) * 4);       // exclusive scan of tot
+    s.fin = take(E * 8);              // first row / rows left per expert
+    s.send = take(kSendStage * 4);    // send counts of this block's source ranks
+    s.misc = take(64 * 4);            // flags and scan partials
     s.bytes = o;
     return s;
 }

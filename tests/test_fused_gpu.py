@@ -46,6 +46,9 @@ CASES = {
     # E = 256, R = 8 (rows of 512 bytes: 147 KB read and written per block)
     "small_max": W.Workload("small_max", N=16, T=32, E=256, R=8, H=256, score_fn=W.SIGMOID,
                             renormalize=True, bias="normal", seed=66),
+    # odd E: the single-cluster path (64 tokens) and the cooperative kernel (960 tokens)
+    "odd_e_small": W.Workload("odd_e_small", N=1, T=64, E=7, R=3, H=64, seed=69),
+    "odd_e_coop": W.Workload("odd_e_coop", N=3, T=320, E=9, R=3, H=64, seed=70),
     # a cluster of one block: one rank, 32 tokens
     "one_block": W.Workload("one_block", N=1, T=32, E=8, R=2, H=64, bias="normal", seed=68),
     # past the cluster path's per-block row traffic (1.2 MB): cooperative kernel

@@ -113,6 +113,12 @@ REDUCED = {
                              seed=9),
     # R > 8 uses the 512-thread count kernel
     "r16": W.Workload("r16", N=4, T=600, E=64, R=16, H=64, score_fn=W.SIGMOID, seed=10),
+    # odd E through each count variant (shared-memory tables read as int2 must
+    # stay 8-byte aligned): 256-thread blocks, 1024-thread blocks (N*T > 4096)
+    # and 512-thread blocks (R > 8)
+    "odd_e_256": W.Workload("odd_e_256", N=5, T=100, E=5, R=2, H=64, cap_rows=125, seed=17),
+    "odd_e_1024": W.Workload("odd_e_1024", N=3, T=2000, E=21, R=5, H=64, seed=18),
+    "odd_e_r17": W.Workload("odd_e_r17", N=1, T=300, E=33, R=17, H=64, score_fn=W.SIGMOID, seed=19),
     # 72 KB bf16 rows: pack and combine run several passes of a 1024-thread
     # block per row, and pack skips its L2 prefetch (rows over 64 KB)
     "wide_rows": W.Workload("wide_rows", N=2, T=24, E=8, R=3, H=36864, renormalize=True,
