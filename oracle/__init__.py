@@ -232,7 +232,8 @@ def x_as_bytes(x):
         a = t.numpy()
     else:
         a = np.ascontiguousarray(x)
-    return a.view(np.uint8).reshape(a.shape[0], -1)
+    # the row width is explicit so that an empty batch keeps its shape (0, bytes)
+    return a.view(np.uint8).reshape(a.shape[0], a.dtype.itemsize * int(np.prod(a.shape[1:])))
 
 
 def run(w, inp, with_combine=True):

@@ -56,7 +56,11 @@ def _setup(w):
 
 @pytest.mark.parametrize("name", ["tiny", "qwen_small", "odd_f32", "odd_bf16", "fp8"])
 def test_pack_rank_writes_only_that_region(name):
-    w = CASES[name]
+    check_pack_rank(CASES[name])
+
+
+def check_pack_rank(w):
+    """Rank N-1's rows equal the oracle's; nothing else is written."""
     inp = W.make_inputs(w)
     gr = GpuRun(w, inp)
     ref = oracle.run(w, inp, with_combine=False)
@@ -82,7 +86,11 @@ def test_pack_rank_writes_only_that_region(name):
 
 @pytest.mark.parametrize("name", list(CASES))
 def test_local_accumulation_per_rank(name):
-    w = CASES[name]
+    check_local_accumulation(CASES[name])
+
+
+def check_local_accumulation(w):
+    """Each rank's local sum against the oracle; all ranks add up to the combine."""
     inp, gr, ref = _setup(w)
     b = gr.bufs
     out_d = torch.empty_like(b.out)
@@ -105,7 +113,12 @@ def test_local_accumulation_per_rank(name):
 
 @pytest.mark.parametrize("name", list(CASES))
 def test_send_side_partials_and_reduction(name):
-    w = CASES[name]
+    check_send_side_partials(CASES[name])
+
+
+def check_send_side_partials(w):
+    """Partial rows and slots against the oracle; their reduction against the
+    oracle's and against the plain combine."""
     inp, gr, ref = _setup(w)
     b = gr.bufs
     s = moe.buffer_sizes(gr.dims)
