@@ -51,7 +51,24 @@ def _shapes(n, seed=20261202):
     return out
 
 
-SHAPES = _shapes(24)
+def _large_shapes(n, seed=77):
+    """Batches of several thousand tokens (the count kernel's 1024-thread
+    blocks and several tiles of tokens per block), narrow rows."""
+    rng = random.Random(seed)
+    out = []
+    for i in range(n):
+        N = rng.choice([1, 2, 3, 4, 8])
+        E = N * rng.choice([1, 3, 5, 16, 32])
+        R = rng.randint(1, min(E, 32))
+        T = rng.randint(4097 // N + 1, 40000 // N)
+        out.append(W.Workload(f"large{i}", N=N, T=T, E=E, R=R, H=8 * rng.randint(1, 8),
+                              score_fn=rng.choice([W.SOFTMAX, W.SIGMOID]),
+                              renormalize=rng.random() < 0.5, bias=rng.choice(["none", "normal"]),
+                              seed=6000 + i))
+    return out
+
+
+SHAPES = _shapes(24) + _large_shapes(6)
 
 
 @pytest.mark.parametrize("w", SHAPES, ids=lambda w: w.name)
