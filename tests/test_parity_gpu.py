@@ -113,6 +113,9 @@ REDUCED = {
                              seed=9),
     # R > 8 uses the 512-thread count kernel
     "r16": W.Workload("r16", N=4, T=600, E=64, R=16, H=64, score_fn=W.SIGMOID, seed=10),
+    # 128 ranks of 2 tokens: a count block's tokens come from so many source
+    # ranks that its send counts go to global atomics instead of shared memory
+    "many_ranks": W.Workload("many_ranks", N=128, T=2, E=256, R=4, H=64, bias="normal", seed=20),
     # odd E through each count variant (shared-memory tables read as int2 must
     # stay 8-byte aligned): 256-thread blocks, 1024-thread blocks (N*T > 4096)
     # and 512-thread blocks (R > 8)
