@@ -49,6 +49,11 @@ CASES = {
     # odd E: the single-cluster path (64 tokens) and the cooperative kernel (960 tokens)
     "odd_e_small": W.Workload("odd_e_small", N=1, T=64, E=7, R=3, H=64, seed=69),
     "odd_e_coop": W.Workload("odd_e_coop", N=3, T=320, E=9, R=3, H=64, seed=70),
+    # 256 tokens with 14 KB rows: too much row traffic for the cluster path, so
+    # the cooperative kernel runs with a single count block
+    "coop_one_count_block": W.Workload("coop_one_count_block", N=2, T=128, E=16, R=4, H=7168,
+                                       score_fn=W.SIGMOID, renormalize=True, bias="normal",
+                                       expert_op=W.EXPERT_SCALE, seed=71),
     # a cluster of one block: one rank, 32 tokens
     "one_block": W.Workload("one_block", N=1, T=32, E=8, R=2, H=64, bias="normal", seed=68),
     # past the cluster path's per-block row traffic (1.2 MB): cooperative kernel
