@@ -237,7 +237,7 @@ int moe_dispatch_pack(const MoeDims *dims, const void *x, const float *x_scales,
                                                      (cudaStream_t)stream),
                            "moe_dispatch_pack");
     return cuda_result(launch_dispatch_pack(x, fp8 ? x_scales : nullptr, pos, v.NT, dims->R, v.x_row_bytes,
-                                            v.scales_per_row, 0, v.rows_total, 1, packed_x,
+                                            v.scales_per_row, v.rows_total, packed_x,
                                             fp8 ? packed_scales : nullptr, packed_src,
                                             (cudaStream_t)stream),
                        "moe_dispatch_pack");
@@ -276,7 +276,7 @@ int moe_combine(const MoeDims *dims, const void *y, const int32_t *pos, const fl
         return set_error(MOE_ERR_INVALID_ARG, "moe_combine: y and out must be 16-byte aligned");
     if (!aligned(pos, 4) || !aligned(topk_w, 4))
         return set_error(MOE_ERR_INVALID_ARG, "moe_combine: pos and topk_w must be 4-byte aligned");
-    return cuda_result(launch_combine(y, dims->y_dtype, pos, topk_w, v.NT, dims->R, dims->H, 0, v.rows_total,
+    return cuda_result(launch_combine(y, dims->y_dtype, pos, topk_w, v.NT, dims->R, dims->H, v.rows_total,
                                       out, (cudaStream_t)stream),
                        "moe_combine");
 }

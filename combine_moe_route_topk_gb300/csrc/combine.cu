@@ -6,11 +6,8 @@
 // "Enabling trillion-parameter models on AWS EFA", section "Evaluation":
 // accumulation happens on the receiving side only, R rows per token.
 //
-// Only pairs whose row lies in [row_lo, row_hi) contribute: the whole
-// receive buffer for the combine, one rank's region for the local
-// accumulation of one rank ("Hosting Qwen on Blackwell", section "Expert
-// parallel": with replicated inputs each rank accumulates its own experts'
-// outputs before an all-reduce).
+// Pairs whose row is negative (dropped by count) or outside the N*cap rows
+// of the receive buffer contribute nothing.
 //
 // HBM stream: R rows gathered per token, one row written.  One block per
 // token at a time; every thread owns 16-byte output vectors and issues the
@@ -31,8 +28,8 @@ constexpr int kCombKB = 8;  // source rows loaded together
 template <int kBf16>
 __global__ void __launch_bounds__(kCombThreads)
 combine_kernel(const uint4 *__restrict__ y, const int32_t *__restrict__ pos,
-               const float *__restrict__ topk_w, int64_t NT, int R, int nvec, int64_t row_lo,
-               int64_t row_hi, uint4 *__restrict__ out) {
+               const float *__restrict__ topk_w, int64_t NT, int R, int nvec, int64_t rows_total,
+               uint4 *__restrict__ out) {
     using VT = Vec<kBf16>;
     constexpr int EL = VT::kElems;
     __shared__ int s_pos[32];
@@ -43,7 +40,7 @@ combine_kernel(const uint4 *__restrict__ y, const int32_t *__restrict__ pos,
     for (int64_t g = blockIdx.x; g < NT; g += gridDim.x) {
         if (tid < R) {
             const int p = __ldg(pos + g * R + tid);
-            s_pos[tid] = ((int64_t)p >= row_lo && (int64_t)p < row_hi) ? p : -1;
+            s_pos[tid] = (p >= 0 && (int64_t)p < rows_total) ? p : -1;
             s_w[tid] = __ldg(topk_w + g * R + tid);
         }
         __syncthreads();
@@ -89,7 +86,7 @@ combine_kernel(const uint4 *__restrict__ y, const int32_t *__restrict__ pos,
 }  // namespace
 
 cudaError_t launch_combine(const void *y, int y_dtype, const int32_t *pos, const float *topk_w,
-                           int64_t NT, int R, int H, int64_t row_lo, int64_t row_hi, void *out,
+                           int64_t NT, int R, int H, int64_t rows_total, void *out,
                            cudaStream_t stream) {
     if (NT == 0) return cudaSuccess;
     const int elem = (y_dtype == MOE_BF16) ? 2 : 4;
@@ -104,7 +101,7 @@ cudaError_t launch_combine(const void *y, int y_dtype, const int32_t *pos, const
     cfg.numAttrs = 1;
     auto kern = (y_dtype == MOE_BF16) ? combine_kernel<1> : combine_kernel<0>;
     return cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const uint4 *>(y), pos, topk_w, NT, R,
-                              nvec, row_lo, row_hi, reinterpret_cast<uint4 *>(out));
+                              nvec, rows_total, reinterpret_cast<uint4 *>(out));
 }
 
 }  // namespace moe

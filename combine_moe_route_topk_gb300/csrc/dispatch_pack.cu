@@ -8,10 +8,8 @@
 // contiguously per destination.  Here the destination regions are
 // partitions of one allocation, so the "send" is the packing store itself.
 //
-// Only pairs whose row lies in [row_lo, row_hi) are copied: all rank
-// regions for the dispatch, one rank's region when a rank selects the
-// tokens routed to its own experts from replicated inputs ("Hosting Qwen on
-// Blackwell", section "Expert parallel").
+// Pairs whose row is negative (dropped by count) or outside the N*cap rows
+// of the receive buffer are skipped.
 //
 // The kernel is a pure HBM stream: each x row is read once and written R
 // times.  One block handles one token at a time and is sized to the row:
@@ -26,8 +24,7 @@
 // blocks use that time to pull the x rows into L2 with bulk prefetches
 // (evict-last) before they wait for count; the R-fold row stores carry an
 // evict-first hint so that they do not push those rows out again.  The
-// prefetch covers at most half of the L2, and is left out for a row window
-// (one rank's rows), which reads only some of the tokens.
+// prefetch covers at most half of the L2.
 #include "mem_ops.cuh"
 #include "moe_internal.cuh"
 #include "pdl.cuh"
@@ -41,7 +38,7 @@ constexpr int kPackMaxThreads = 1024;
 __global__ void __launch_bounds__(kPackMaxThreads)
 dispatch_pack_kernel(const uint4 *__restrict__ x, const float *__restrict__ x_scales,
                      const int32_t *__restrict__ pos, int64_t NT, int R, int nvec, int spr,
-                     int64_t row_lo, int64_t row_hi, int64_t pf_rows, int pf_blocks,
+                     int64_t rows_total, int64_t pf_rows, int pf_blocks,
                      uint4 *__restrict__ packed_x, float *__restrict__ packed_scales,
                      int32_t *__restrict__ packed_src) {
     __shared__ int s_pos[32];
@@ -53,12 +50,12 @@ dispatch_pack_kernel(const uint4 *__restrict__ x, const float *__restrict__ x_sc
     for (int64_t g = blockIdx.x; g < NT; g += gridDim.x) {
         if (tid < R) {
             const int p = __ldg(pos + g * R + tid);
-            const bool ok = (int64_t)p >= row_lo && (int64_t)p < row_hi;
+            const bool ok = p >= 0 && (int64_t)p < rows_total;
             s_pos[tid] = ok ? p : -1;
             if (ok) packed_src[p] = (int32_t)(g * R + tid);
         }
         __syncthreads();
-        bool any = false;  // a token with no pair in the window is not read
+        bool any = false;  // a token whose pairs were all dropped is not read
         for (int k = 0; k < R; ++k) any |= s_pos[k] >= 0;
         const uint4 *src = x + g * nvec;
         for (int c0 = tid; any && c0 < nvec; c0 += nthr * kPackVecs) {
@@ -94,7 +91,7 @@ dispatch_pack_kernel(const uint4 *__restrict__ x, const float *__restrict__ x_sc
 
 cudaError_t launch_dispatch_pack(const void *x, const float *x_scales, const int32_t *pos,
                                  int64_t NT, int R, int64_t row_bytes, int scales_per_row,
-                                 int64_t row_lo, int64_t row_hi, int prefetch_x, void *packed_x,
+                                 int64_t rows_total, void *packed_x,
                                  float *packed_scales, int32_t *packed_src, cudaStream_t stream) {
     if (NT == 0) return cudaSuccess;
     const int nvec = (int)(row_bytes / 16);
@@ -104,9 +101,8 @@ cudaError_t launch_dispatch_pack(const void *x, const float *x_scales, const int
     int64_t threads = ((nvec + kPackVecs - 1) / kPackVecs + 31) / 32 * 32;
     if (threads < 32) threads = 32;
     if (threads > kPackMaxThreads) threads = kPackMaxThreads;
-    // prefetch (whole dispatch only): rows filling at most half the L2,
-    // issued by one block per SM
-    int64_t pf_rows = (prefetch_x && row_bytes <= 65536) ? (l2_bytes() / 2) / row_bytes : 0;
+    // prefetch: rows filling at most half the L2, issued by one block per SM
+    int64_t pf_rows = row_bytes <= 65536 ? (l2_bytes() / 2) / row_bytes : 0;
     if (pf_rows > NT) pf_rows = NT;
     int64_t pf_blocks = sm_count();
     if (pf_blocks > grid) pf_blocks = grid;
@@ -119,7 +115,7 @@ cudaError_t launch_dispatch_pack(const void *x, const float *x_scales, const int
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, dispatch_pack_kernel, reinterpret_cast<const uint4 *>(x),
-                              x_scales, pos, NT, R, nvec, scales_per_row, row_lo, row_hi,
+                              x_scales, pos, NT, R, nvec, scales_per_row, rows_total,
                               pf_rows, (int)pf_blocks, reinterpret_cast<uint4 *>(packed_x),
                               packed_scales, packed_src);
 }

@@ -31,8 +31,8 @@ cudaError_t launch_dispatch_count(const int32_t *topk_idx, int N, int T, int E, 
 // Pairs whose row lies outside [row_lo, row_hi) are skipped.
 cudaError_t launch_dispatch_pack(const void *x, const float *x_scales, const int32_t *pos,
                                  int64_t NT, int R, int64_t row_bytes, int scales_per_row,
-                                 int64_t row_lo, int64_t row_hi, int prefetch_x, void *packed_x,
-                                 float *packed_scales, int32_t *packed_src, cudaStream_t stream);
+                                 int64_t rows_total, void *packed_x, float *packed_scales,
+                                 int32_t *packed_src, cudaStream_t stream);
 
 // Bulk-copy pack (whole rows through shared memory); rows of more than
 // 48 KB are not supported (pack_bulk_stages returns 0).
@@ -82,7 +82,7 @@ cudaError_t launch_dispatch_pack_quant(const void *x, const int32_t *pos, int64_
 
 // Pairs whose row lies outside [row_lo, row_hi) contribute nothing.
 cudaError_t launch_combine(const void *y, int y_dtype, const int32_t *pos, const float *topk_w,
-                           int64_t NT, int R, int H, int64_t row_lo, int64_t row_hi, void *out,
+                           int64_t NT, int R, int H, int64_t rows_total, void *out,
                            cudaStream_t stream);
 
 // Expert-parallel local path of one rank (rows [row_lo, row_hi) only).
