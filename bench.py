@@ -570,6 +570,24 @@ def run_ours(args):
     except moe.MoeError as ex:
         fused = {"unsupported": str(ex)}
 
+    # the router with the bias in the selection key only (score of the raw
+    # logit + bias decides; weights are the raw scores), against the default
+    rtimes = {}
+    for label, fn in (("default", w.score_fn), ("bias_select_only", w.score_fn | moe.MOE_BIAS_SELECT_ONLY)):
+        rpool = [new_events(2) for _ in range(nb + 3)]
+        host_lead(nb + 3)
+        for i in range(nb + 3):
+            flush()
+            rpool[i][0].record(stream)
+            moe.route_topk(dims, inp.logits, inp.bias, fn, w.renormalize, b.topk_idx, b.topk_w, stream)
+            rpool[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        rtimes[label] = statistics.mean(a.elapsed_time(c) for a, c in rpool[3:])
+    # restore the default routing for the steps below
+    launch("route")
+    launch("count")
+    torch.cuda.synchronize(dev)
+
     # send-side accumulation (partial rows per token and destination rank,
     # then their sum) and the expert-parallel local path of one rank
     next_rows = {}
@@ -598,6 +616,10 @@ def run_ours(args):
     t_red = statistics.mean(e[1].elapsed_time(e[2]) for e in evs2)
     b_part = w.NT * (yb * w.R + yb * P) + w.NT * w.R * 8
     b_red = yb * used + w.NT * yb + w.NT * P * 4
+    next_rows["route_bias_select_only"] = {
+        "ms": rtimes["bias_select_only"], "default_route_ms": rtimes["default"],
+        "note": "moe_route_topk with MOE_BIAS_SELECT_ONLY (DeepSeek-V3 convention) vs the "
+                "default reading, each timed alone after an L2 flush"}
     next_rows["send_side_combine"] = {
         "partials_ms": t_part, "reduce_ms": t_red, "ms": t_part + t_red,
         "alg_bytes": b_part + b_red, "alg_gbs": (b_part + b_red) / ((t_part + t_red) / 1e3) / 1e9,
