@@ -369,7 +369,7 @@ int moe_dispatch_fused(const MoeDims *dims, const float *logits, const float *bi
     if (rc != MOE_OK) return rc;
     if (!valid_score_fn(score_fn))
         return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_fused: unknown score_fn %d", score_fn);
-    const char *why = fused_unsupported(dims->N, dims->T, dims->E, dims->R);
+    const char *why = fused_unsupported(dims->N, dims->T, dims->E, dims->R, v.x_row_bytes);
     if (why[0] != '\0')
         return set_error(MOE_ERR_UNSUPPORTED, "moe_dispatch_fused: %s; use the separate calls", why);
     const bool fp8 = dims->x_dtype == MOE_FP8E4M3_BLK128;
@@ -393,7 +393,8 @@ int moe_dispatch_fused(const MoeDims *dims, const float *logits, const float *bi
                                           fp8 ? packed_scales : nullptr, packed_src, workspace,
                                           (cudaStream_t)stream);
     if (e == cudaErrorNotSupported || e == cudaErrorCooperativeLaunchTooLarge)
-        return set_error(MOE_ERR_UNSUPPORTED, "moe_dispatch_fused: the device cannot hold enough co-resident blocks");
+        return set_error(MOE_ERR_UNSUPPORTED, "moe_dispatch_fused: the device cannot run this batch fused "
+                                              "(cluster or co-resident blocks unavailable)");
     return cuda_result(e, "moe_dispatch_fused");
 }
 
@@ -406,7 +407,7 @@ int moe_dispatch_fused_static(const MoeDims *dims, const float *logits, const fl
     Derived v;
     int rc = check_dims(dims, &v, "moe_dispatch_fused_static");
     if (rc != MOE_OK) return rc;
-    const char *why = fused_unsupported(dims->N, dims->T, dims->E, dims->R);
+    const char *why = fused_unsupported(dims->N, dims->T, dims->E, dims->R, v.x_row_bytes);
     if (why[0] != '\0')
         return set_error(MOE_ERR_UNSUPPORTED, "moe_dispatch_fused_static: %s; use the separate calls", why);
     const int64_t need = fused_workspace_bytes(dims->E);

@@ -499,7 +499,9 @@ int64_t fused_workspace_bytes(int E) {
 }
 
 // Empty string when the fused kernel handles these dimensions, else why not.
-const char *fused_unsupported(int N, int T, int E, int R) {
+namespace {
+// Limits of the cooperative kernel ("" when it can run the batch).
+const char *cooperative_unsupported(int N, int T, int E, int R) {
     const int64_t NT = (int64_t)N * T;
     if (R > kFMaxR) return "R > 8";
     if (E > 512) return "E > 512";
@@ -507,6 +509,14 @@ const char *fused_unsupported(int N, int T, int E, int R) {
     if (NT > (int64_t)kMaxCountBlocks * kFThreads) return "N*T > 4096 (not a decode batch)";
     if (NT > 0 && (int64_t)(kFThreads / T + 2) * N > kSendStage) return "too many ranks per count block";
     return "";
+}
+}  // namespace
+
+// A batch runs fused if the single-cluster kernel takes it (no limit on T
+// or R beyond the interface's) or else the cooperative kernel does.
+const char *fused_unsupported(int N, int T, int E, int R, int64_t row_bytes) {
+    if (dispatch_small_eligible((int64_t)N * T, E, R, row_bytes)) return "";
+    return cooperative_unsupported(N, T, E, R);
 }
 
 cudaError_t launch_dispatch_fused(const float *logits, const float *bias, int score_fn, int renormalize,
@@ -525,6 +535,9 @@ cudaError_t launch_dispatch_fused(const float *logits, const float *bias, int sc
                                               expert_offsets, rank_counts, rank_offsets, send_counts, pos,
                                               status, packed_x, packed_scales, packed_src, stream);
         if (e != cudaErrorNotSupported) return e;
+        // the device cannot schedule the cluster: the cooperative kernel, if
+        // the batch is within its limits
+        if (cooperative_unsupported(N, T, E, R)[0] != '\0') return cudaErrorNotSupported;
     }
     FusedParams P;
     P.logits = logits;

@@ -48,7 +48,7 @@ cudaError_t take_device_error(int *err, cudaStream_t stream);
 
 // Decode-fused route + count + pack (one cooperative launch).
 int64_t fused_workspace_bytes(int E);
-const char *fused_unsupported(int N, int T, int E, int R);  // "" when supported
+const char *fused_unsupported(int N, int T, int E, int R, int64_t row_bytes);  // "" when supported
 cudaError_t launch_dispatch_fused(const float *logits, const float *bias, int score_fn, int renormalize,
                                   const void *x, const float *x_scales, int N, int T, int E, int R,
                                   int64_t row_bytes, int spr, int64_t cap, int32_t *topk_idx,

@@ -192,16 +192,17 @@ int moe_dispatch_pack(const MoeDims *dims, const void *x, const float *x_scales,
  *   workspace  device scratch of MoeSizes.fused_workspace_bytes bytes,
  *              16-byte aligned, owned by the caller; calls that may run at
  *              the same time need separate workspaces.
- * Decode batches only: N*T <= 4096, T % 32 == 0, R <= 8, E <= 512 (else
- * MOE_ERR_UNSUPPORTED before anything is enqueued: use the three calls).
- * Batches of at most 512 tokens with E <= 256 and at most 1 MB of rows
- * read and written per 32 tokens (32 * (1 + R) * row bytes) run as one
- * thread-block cluster whose blocks own 32 tokens each and exchange only
- * per-expert counts through distributed shared memory (no grid barrier; the
- * workspace is not touched).  Other batches run as a cooperative launch
- * (all its blocks are resident at once) whose phases meet at grid-wide
- * barriers; each barrier wait is bounded, and one that gives up leaves
- * MOE_ERR_TIMEOUT in *status.  On GB300 the fused call beats the three
+ * Decode batches only, in one of two forms (else MOE_ERR_UNSUPPORTED before
+ * anything is enqueued: use the three calls):
+ *   - N*T <= 512, E <= 256 and at most 1 MB of rows read and written per 32
+ *     tokens (32 * (1 + R) * row bytes), any T and R: one thread-block
+ *     cluster whose blocks own 32 tokens each and exchange only per-expert
+ *     counts through distributed shared memory (no grid barrier; the
+ *     workspace is not touched);
+ *   - otherwise N*T <= 4096, T % 32 == 0, R <= 8, E <= 512: a cooperative
+ *     launch (all its blocks are resident at once) whose phases meet at
+ *     grid-wide barriers; each barrier wait is bounded, and one that gives
+ *     up leaves MOE_ERR_TIMEOUT in *status.  On GB300 the fused call beats the three
  * separate calls only for small rows (up to about 200 KB of row traffic
  * per 32 tokens, e.g. 256 tokens with R = 2 and 2 KB rows: 12.4 vs 15.4 us);
  * beyond that the separate calls, whose pack uses every SM, are faster. */

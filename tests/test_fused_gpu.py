@@ -54,6 +54,11 @@ CASES = {
     "coop_one_count_block": W.Workload("coop_one_count_block", N=2, T=128, E=16, R=4, H=7168,
                                        score_fn=W.SIGMOID, renormalize=True, bias="normal",
                                        expert_op=W.EXPERT_SCALE, seed=71),
+    # shapes only the single-cluster path takes: one token per rank (T % 32
+    # != 0) and R > 8
+    "decode_t1": W.Workload("decode_t1", N=64, T=1, E=128, R=8, H=256, score_fn=W.SIGMOID,
+                            renormalize=True, bias="normal", seed=72),
+    "r12_t24": W.Workload("r12_t24", N=8, T=24, E=64, R=12, H=128, renormalize=True, seed=73),
     # a cluster of one block: one rank, 32 tokens
     "one_block": W.Workload("one_block", N=1, T=32, E=8, R=2, H=64, bias="normal", seed=68),
     # past the cluster path's per-block row traffic (1.2 MB): cooperative kernel
@@ -73,7 +78,8 @@ def test_fused_cases(name):
 # dsv3_decode and past_small take the cooperative kernel; tiny and small_max
 # the single thread-block cluster (up to 512 tokens, E <= 256, at most 1 MB of
 # rows read and written per 32 tokens)
-@pytest.mark.parametrize("name", ["dsv3_decode", "past_small", "tiny", "small_max"])
+@pytest.mark.parametrize("name", ["dsv3_decode", "past_small", "tiny", "small_max", "decode_t1",
+                                  "r12_t24"])
 def test_fused_equals_separate_calls_bytewise(name):
     w = W.WORKLOADS.get(name) or CASES[name]
     inp = W.make_inputs(w)
