@@ -63,7 +63,30 @@ def _fused_shapes(n, seed=31):
     return out
 
 
-@pytest.mark.parametrize("w", _fused_shapes(16), ids=lambda w: w.name)
+def _small_fused_shapes(n, seed=33):
+    """Batches only the single-cluster path takes: any T, R up to 32."""
+    rng = random.Random(seed)
+    out = []
+    for i in range(n):
+        N = rng.choice([1, 2, 4, 8, 16, 64])
+        E = N * rng.choice([1, 2, 3, 4])
+        while E > 256:
+            E //= 2
+        E = max(N, E // N * N)
+        R = rng.randint(1, min(E, 32))
+        T = rng.randint(1, max(1, 512 // N))
+        x_dtype, H, y_dtype, op = _rows(rng)
+        H = min(H, 256)  # keep the rows within the cluster path's traffic limit
+        if x_dtype == W.FP8E4M3_BLK128:
+            H = 128
+        out.append(W.Workload(f"small{i}", N=N, T=T, E=E, R=R, H=H, x_dtype=x_dtype, y_dtype=y_dtype,
+                              expert_op=op, score_fn=rng.choice([W.SOFTMAX, W.SIGMOID]),
+                              renormalize=rng.random() < 0.5, bias=rng.choice(["none", "normal"]),
+                              seed=2500 + i))
+    return out
+
+
+@pytest.mark.parametrize("w", _fused_shapes(16) + _small_fused_shapes(12), ids=lambda w: w.name)
 def test_random_fused_equals_separate_calls(w):
     inp = W.make_inputs(w)
     try:
