@@ -132,7 +132,7 @@ using namespace moe;
 
 extern "C" {
 
-int moe_version(void) { return 10000; }
+int moe_version(void) { return MOE_VERSION; }
 
 const char *moe_last_error(void) { return g_err; }
 

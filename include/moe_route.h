@@ -342,7 +342,12 @@ int moe_take_device_error(void *stream);
 /* Message for the last error returned in the calling thread ("" if none). */
 const char *moe_last_error(void);
 
-/* Library ABI version (major*10000 + minor*100 + patch). */
+/* Library ABI version (major*10000 + minor*100 + patch).  1.1: the
+ * MOE_BIAS_SELECT_ONLY flag, moe_dispatch_fused_static,
+ * moe_selftest_bounded_wait, the single-cluster fused path and H <= 2^24.
+ * A caller can compare MOE_VERSION (the header it was built against) with
+ * moe_version() (the library it loaded). */
+#define MOE_VERSION 10100
 int moe_version(void);
 
 #ifdef __cplusplus
