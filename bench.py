@@ -111,7 +111,8 @@ def source_hash(name: str) -> str:
             data = fh.read()
         part = data
         if f in DECLARATION_HEADERS:
-            part = b"\n".join(l for l in data.splitlines() if l.lstrip().startswith(b"#define"))
+            part = b"\n".join(l for l in data.splitlines() if l.lstrip().startswith(b"#define")
+                              and not re.match(rb"\s*#define\s+MOE_VERSION\b", l))
         h.update(f.encode() + b"\0" + part)
         todo += [m.decode() for m in re.findall(rb'#include "([^"]+)"', data)]
     return h.hexdigest()[:16]

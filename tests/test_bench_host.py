@@ -38,6 +38,8 @@ def test_source_hash_follows_headers_but_not_declarations(tmp_path, monkeypatch)
     # a new host declaration in either declaration header: same kernel
     assert _hash(tmp_path / "b", monkeypatch, internal=INTERNAL + "int launch_b(int);\n") == base
     assert _hash(tmp_path / "c", monkeypatch, public=PUBLIC + "int moe_b(void);\n") == base
+    # the library version is not kernel input either
+    assert _hash(tmp_path / "f", monkeypatch, public=PUBLIC + "#define MOE_VERSION 10200\n") == base
     # a changed constant the kernel can see, or a changed kernel line: different
     assert _hash(tmp_path / "d", monkeypatch, public=PUBLIC.replace("MOE_OK 0", "MOE_OK 1")) != base
     assert _hash(tmp_path / "e", monkeypatch, kernel=KERNEL + "// edit\n") != base
