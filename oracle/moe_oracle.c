@@ -19,6 +19,7 @@
  *        "Quantization".
  *   [P2] "Efficient and portable mixture-of-experts communication", sections
  *        "Introduction", "Portable kernels", "Dispatch", "Combine".
+ *   [P4] "Hosting Qwen on Blackwell", section "Expert parallel".
  *   [P5] "Enabling trillion-parameter models on AWS EFA", sections "Send and
  *        receive buffers", "Dispatch and combine", "Evaluation".
  *
