@@ -19,15 +19,24 @@
 //      at a barrier of their own, then each derives offsets, send counts and
 //      the rows of its tokens;
 //   3. pack: every block copies token rows (grid-stride) to their rows.
-// Each block's first token row is loaded before phase 1 ends (x is an
-// input, not written here).  Every barrier wait is bounded: a wait that
-// gives up makes the status word MOE_ERR_TIMEOUT and the kernel returns.
+// x is an input, not written here: while the count blocks work, the other
+// blocks (idle until the second barrier) ask for the x rows to be brought
+// into L2 (bulk prefetch, evict-last, at most half of the L2), so that
+// pack reads them from L2, and the packed rows are stored with an
+// evict-first hint so that they do not push those rows out.  Measured on
+// the DeepSeek-V3 decode batch (GB300, L2 flushed before each launch):
+// pack phase 65 -> 56 us, count phase 12 -> 18 us (its L2 accesses queue
+// behind the prefetch), whole kernel 118 -> 115 us; issued before routing
+// instead, the prefetches slowed routing from 5.5 to 14 us.  Every barrier
+// wait is bounded: a wait that gives up makes the status word
+// MOE_ERR_TIMEOUT and the kernel returns.
 //
 // Scope: decode batches (N*T <= 4096), T % 32 == 0, R <= 8, E <= 512; the
 // host rejects anything else with MOE_ERR_UNSUPPORTED (use the three
 // separate calls).
 #include <mutex>
 
+#include "mem_ops.cuh"
 #include "moe_internal.cuh"
 #include "route_impl.cuh"
 
@@ -56,6 +65,7 @@ struct FusedParams {
     int nvec, spr;
     int N, T, E, R, cap, CB;
     int64_t rows_total;
+    int64_t pf_rows;  // x rows [0, pf_rows) are prefetched into L2 (0: none)
     int32_t *topk_idx;
     float *topk_w;
     int32_t *expert_counts, *expert_offsets, *rank_counts, *rank_offsets, *send_counts, *pos,
@@ -109,14 +119,6 @@ __device__ bool bounded_barrier(int *arrive, int *gen, int nblocks, int *err) {
     return s_ok != 0;
 }
 
-__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
 __device__ __forceinline__ unsigned lanemask_lt() {
     unsigned m;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
@@ -148,10 +150,13 @@ __host__ __device__ inline FusedSmem fused_smem_layout(int E) {
     return s;
 }
 
-constexpr int kPre = 4;  // 16-byte vectors of the first row kept per thread
+constexpr int kPackU = 4;  // 16-byte vectors of a row per thread in flight (pack)
 
+// 3 co-resident blocks per SM.  4 (64 registers per thread, no spills for
+// up to 8 experts per lane) routes a 4096-token batch in one pass, but the
+// whole kernel took longer on the DeepSeek-V3 decode batch (123 vs 115 us).
 template <int J, bool kVec4>
-__global__ void __launch_bounds__(kFThreads, 3)  // 3 co-resident blocks per SM
+__global__ void __launch_bounds__(kFThreads, 3)
 dispatch_fused_kernel(FusedParams P) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_pos[kFMaxR];
@@ -163,21 +168,17 @@ dispatch_fused_kernel(FusedParams P) {
     for (int64_t g = (int64_t)blockIdx.x * kFWarps + warp; g < NT; g += (int64_t)gridDim.x * kFWarps)
         route_impl::route_token<J, kVec4>(P.logits, P.bias, g, P.E, P.R, P.score_fn,
                                           P.renormalize, P.topk_idx, P.topk_w, lane);
-    // first token row of this block (an input: safe to read at any time)
-    uint4 pre[kPre];
-    const int64_t g_first = blockIdx.x;
-    const bool preload = g_first < NT && P.nvec <= kFThreads * kPre;
-    if (preload) {
-#pragma unroll
-        for (int u = 0; u < kPre; ++u) {
-            const int c = tid + u * kFThreads;
-            if (c < P.nvec) pre[u] = ld_stream(P.x + g_first * P.nvec + c);
-        }
-    }
     bool alive = bounded_barrier(P.ws + kWsGridArrive, P.ws + kWsGridGen, gridDim.x, err);
 
     // ---- phase 2: count (blocks 0 .. CB-1) -------------------------------------
     const int b = blockIdx.x;
+    // meanwhile the other blocks prefetch x, one row per lane of warp 0
+    const int nb = (int)gridDim.x - P.CB;
+    if (alive && b >= P.CB && warp == 0) {
+        const uint64_t keep = l2_policy_evict_last();
+        for (int64_t r = (b - P.CB) + (int64_t)lane * nb; r < P.pf_rows; r += 32ll * nb)
+            prefetch_l2(P.x + r * P.nvec, (uint32_t)P.nvec * 16u, keep);
+    }
     if (alive && b < P.CB) {
         const int E = P.E, N = P.N, T = P.T, R = P.R, L = E / N, CB = P.CB;
         const FusedSmem lay = fused_smem_layout(E);
@@ -411,6 +412,7 @@ dispatch_fused_kernel(FusedParams P) {
 
     // ---- phase 3: pack --------------------------------------------------------
     if (alive) {
+        const uint64_t stream_out = l2_policy_evict_first();
         for (int64_t g = blockIdx.x; g < NT; g += gridDim.x) {
             if (tid < P.R) {
                 const int p = __ldcg(P.pos + g * P.R + tid);  // written in phase 2
@@ -419,22 +421,21 @@ dispatch_fused_kernel(FusedParams P) {
                 if (ok) P.packed_src[p] = (int32_t)(g * P.R + tid);
             }
             __syncthreads();
-            for (int c0 = tid; c0 < P.nvec; c0 += kFThreads * kPre) {
-                uint4 v[kPre];
+            for (int c0 = tid; c0 < P.nvec; c0 += kFThreads * kPackU) {
+                uint4 v[kPackU];
 #pragma unroll
-                for (int u = 0; u < kPre; ++u) {
+                for (int u = 0; u < kPackU; ++u) {
                     const int c = c0 + u * kFThreads;
-                    if (preload && g == g_first) v[u] = pre[u];
-                    else if (c < P.nvec) v[u] = ld_stream(P.x + g * P.nvec + c);
+                    if (c < P.nvec) v[u] = ld_stream(P.x + g * P.nvec + c);
                 }
                 for (int k = 0; k < P.R; ++k) {
                     const int p = s_pos[k];
                     if (p < 0) continue;
                     uint4 *dst = P.packed_x + (int64_t)p * P.nvec;
 #pragma unroll
-                    for (int u = 0; u < kPre; ++u) {
+                    for (int u = 0; u < kPackU; ++u) {
                         const int c = c0 + u * kFThreads;
-                        if (c < P.nvec) dst[c] = v[u];
+                        if (c < P.nvec) st_evict_first(dst + c, v[u], stream_out);
                     }
                 }
             }
@@ -467,6 +468,11 @@ cudaError_t launch_fused_jv(FusedParams P, cudaStream_t stream) {
     const int need = (NT + kFWarps - 1) / kFWarps;  // one routing warp per token is plenty
     if (grid > need) grid = need;
     if (grid < P.CB) return cudaErrorNotSupported;
+    // L2 prefetch of x: rows of at most 64 KB filling at most half the L2
+    const int64_t row_bytes = (int64_t)P.nvec * 16;
+    P.pf_rows = row_bytes <= 65536 ? (l2_bytes() / 2) / row_bytes : 0;
+    if (P.pf_rows > NT) P.pf_rows = NT;
+    if (P.pf_rows < 0) P.pf_rows = 0;
     e = cudaMemsetAsync(P.ws, 0, kWsHeader * sizeof(int), stream);  // barrier words
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
