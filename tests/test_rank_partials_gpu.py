@@ -60,28 +60,33 @@ def test_pack_rank_writes_only_that_region(name):
 
 
 def check_pack_rank(w):
-    """Rank N-1's rows equal the oracle's; nothing else is written."""
+    """Each rank's rows equal the oracle's, and nothing outside them is written
+    (every rank for N <= 8, else the first, second, middle and last)."""
     inp = W.make_inputs(w)
     gr = GpuRun(w, inp)
     ref = oracle.run(w, inp, with_combine=False)
     b, cap = gr.bufs, gr.cap
-    d = w.N - 1
-    b.packed_x.view(torch.uint8).fill_(0xA5)
-    b.packed_src.fill_(-7)
-    moe.dispatch_pack_rank(gr.dims, d, gr.d.x, gr.d.x_scales, b.pos, b.packed_x,
-                           b.packed_scales, b.packed_src)
-    torch.cuda.synchronize()
-    n_d = int(ref["rank_counts"][d])
-    rows = np.arange(d * cap, d * cap + min(n_d, cap))
-    crow = compact_of_region(rows, cap, ref["rank_offsets"])
-    rt = torch.from_numpy(rows).to(b.packed_x.device)
-    np.testing.assert_array_equal(oracle.x_as_bytes(b.packed_x[rt].cpu()), ref["packed_x"][crow])
-    np.testing.assert_array_equal(b.packed_src[rt].cpu().numpy(), ref["packed_src"][crow])
-    if b.packed_scales is not None:
-        np.testing.assert_array_equal(b.packed_scales[rt].cpu().numpy(), ref["packed_scales"][crow])
-    others = torch.ones(b.packed_src.numel(), dtype=torch.bool, device=rt.device)
-    others[rt] = False
-    assert bool((b.packed_src[others] == -7).all())
+    ranks = range(w.N) if w.N <= 8 else [0, 1, w.N // 2, w.N - 1]
+    for d in ranks:
+        b.packed_x.view(torch.uint8).fill_(0xA5)
+        b.packed_src.fill_(-7)
+        moe.dispatch_pack_rank(gr.dims, d, gr.d.x, gr.d.x_scales, b.pos, b.packed_x,
+                               b.packed_scales, b.packed_src)
+        torch.cuda.synchronize()
+        n_d = int(ref["rank_counts"][d])
+        rows = np.arange(d * cap, d * cap + min(n_d, cap))
+        crow = compact_of_region(rows, cap, ref["rank_offsets"])
+        rt = torch.from_numpy(rows).to(b.packed_x.device)
+        np.testing.assert_array_equal(oracle.x_as_bytes(b.packed_x[rt].cpu()), ref["packed_x"][crow],
+                                      err_msg=f"rank {d}")
+        np.testing.assert_array_equal(b.packed_src[rt].cpu().numpy(), ref["packed_src"][crow],
+                                      err_msg=f"rank {d}")
+        if b.packed_scales is not None:
+            np.testing.assert_array_equal(b.packed_scales[rt].cpu().numpy(),
+                                          ref["packed_scales"][crow], err_msg=f"rank {d}")
+        others = torch.ones(b.packed_src.numel(), dtype=torch.bool, device=rt.device)
+        others[rt] = False
+        assert bool((b.packed_src[others] == -7).all()), f"rank {d}"
 
 
 @pytest.mark.parametrize("name", list(CASES))
