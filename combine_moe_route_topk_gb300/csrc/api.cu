@@ -411,7 +411,7 @@ int moe_dispatch_fused_static(const MoeDims *dims, const float *logits, const fl
     if (why[0] != '\0')
         return set_error(MOE_ERR_UNSUPPORTED, "moe_dispatch_fused_static: %s; use the separate calls", why);
     const int64_t need = fused_workspace_bytes(dims->E);
-    if (need > fused_static_scratch_bytes())
+    if (v.NT > 0 && need > fused_static_scratch_bytes())  // an empty batch uses no scratch
         return set_error(MOE_ERR_UNSUPPORTED,
                          "moe_dispatch_fused_static: E=%d needs %lld bytes of scratch; the library's static "
                          "array holds %lld", dims->E, (long long)need, (long long)fused_static_scratch_bytes());

@@ -521,6 +521,7 @@ const char *cooperative_unsupported(int N, int T, int E, int R) {
 // A batch runs fused if the single-cluster kernel takes it (no limit on T
 // or R beyond the interface's) or else the cooperative kernel does.
 const char *fused_unsupported(int N, int T, int E, int R, int64_t row_bytes) {
+    if ((int64_t)N * T == 0) return "";  // empty batch: only the (zero) counts are written
     if (dispatch_small_eligible((int64_t)N * T, E, R, row_bytes)) return "";
     return cooperative_unsupported(N, T, E, R);
 }
@@ -532,6 +533,11 @@ cudaError_t launch_dispatch_fused(const float *logits, const float *bias, int sc
                                   int32_t *rank_counts, int32_t *rank_offsets, int32_t *send_counts,
                                   int32_t *pos, int32_t *status, void *packed_x, float *packed_scales,
                                   int32_t *packed_src, void *workspace, cudaStream_t stream) {
+    // An empty batch has nothing to route or pack: the count step alone
+    // writes its zero counts and offsets and MOE_OK, as the separate calls do.
+    if ((int64_t)N * T == 0)
+        return launch_dispatch_count(topk_idx, N, T, E, R, cap, expert_counts, expert_offsets, rank_counts,
+                                     rank_offsets, send_counts, pos, status, stream);
     // Small batches: one thread-block cluster, no grid barriers and no
     // workspace (the cooperative kernel below handles everything else, and
     // takes over if the device cannot schedule the cluster).

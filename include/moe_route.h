@@ -205,7 +205,9 @@ int moe_dispatch_pack(const MoeDims *dims, const void *x, const float *x_scales,
  *     up leaves MOE_ERR_TIMEOUT in *status.  On GB300 the fused call beats the three
  * separate calls only for small rows (up to about 200 KB of row traffic
  * per 32 tokens, e.g. 256 tokens with R = 2 and 2 KB rows: 12.4 vs 15.4 us);
- * beyond that the separate calls, whose pack uses every SM, are faster. */
+ * beyond that the separate calls, whose pack uses every SM, are faster.
+ * An empty batch (N*T == 0) is always accepted: like moe_dispatch_count it
+ * writes zero counts and offsets and MOE_OK (the workspace is not touched). */
 int moe_dispatch_fused(const MoeDims *dims, const float *logits, const float *bias, int score_fn,
                        int renormalize, const void *x, const float *x_scales, int32_t *topk_idx,
                        float *topk_w, int32_t *expert_counts, int32_t *expert_offsets,

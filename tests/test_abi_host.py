@@ -133,6 +133,19 @@ def test_fused_dispatch_rejects_non_decode_shapes(lib):
         assert why in lib.moe_last_error().decode()
 
 
+def test_fused_dispatch_accepts_empty_batches_of_any_shape(lib):
+    # the shape check passes (an empty batch only runs the count step); with
+    # no GPU the call then fails, if at all, only at the CUDA level
+    P = ctypes.c_void_p
+    ok = P(0x10000)
+    args = [ok] * 16
+    d = moe.make_dims(N=4, T=0, E=64, R=16, H=128)
+    rc = lib.moe_dispatch_fused(ctypes.byref(d), None, None, 0, 0, None, None, *args[:11], None,
+                                ok, ok, None)
+    assert rc != moe.MOE_ERR_INVALID_ARG
+    assert "use the separate calls" not in lib.moe_last_error().decode()
+
+
 def test_rows_wider_than_2_24_elements_are_unsupported(lib):
     d = moe.make_dims(2, 8, 4, 2, (1 << 24) + 8)
     s = moe.MoeSizes()

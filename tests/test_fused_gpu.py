@@ -91,3 +91,30 @@ def test_fused_equals_separate_calls_bytewise(name):
     pb, _, sb = b.packed_rows()
     np.testing.assert_array_equal(pa, pb)
     np.testing.assert_array_equal(sa, sb)
+
+
+@pytest.mark.parametrize("static", [False, True])
+@pytest.mark.parametrize("R", [2, 16])  # R = 16 is past both fused kernels' limits
+def test_fused_empty_batch(static, R):
+    """N*T == 0 is always accepted: zero counts and offsets, MOE_OK, as the
+    separate calls give."""
+    w = W.Workload("empty", N=4, T=0, E=32, R=R, H=64)
+    dims = moe.dims_of(w)
+    b = moe.Buffers(dims)
+    for t in (b.expert_counts, b.expert_offsets, b.rank_counts, b.rank_offsets, b.send_counts):
+        t.fill_(7)
+    b.status.fill_(-99)
+    x = torch.empty(0, w.H, dtype=torch.bfloat16, device="cuda")
+    logits = torch.empty(0, w.E, dtype=torch.float32, device="cuda")
+    args = (dims, logits, None, W.SOFTMAX, False, x, None, b.topk_idx, b.topk_w, b.expert_counts,
+            b.expert_offsets, b.rank_counts, b.rank_offsets, b.send_counts, b.pos, b.status,
+            b.packed_x, None, b.packed_src)
+    if static:
+        moe.dispatch_fused_static(*args)
+    else:
+        ws = torch.empty(moe.buffer_sizes(dims)["fused_workspace_bytes"], dtype=torch.uint8,
+                         device="cuda")
+        moe.dispatch_fused(*args, ws)
+    assert moe.read_status(b.status) == moe.MOE_OK
+    for t in (b.expert_counts, b.expert_offsets, b.rank_counts, b.rank_offsets, b.send_counts):
+        assert int(t.abs().sum()) == 0
