@@ -188,3 +188,16 @@ def test_binding_refuses_cpu_tensors(lib):
     t = torch.zeros(4, 8)
     with pytest.raises(ValueError, match="CUDA tensor"):
         moe.route_topk(d, t, None, 0, False, t, t)
+
+
+def test_rank_entries_reject_ranks_outside_the_batch(lib):
+    P = ctypes.c_void_p
+    ok = P(0x10000)
+    d = moe.make_dims(N=4, T=8, E=8, R=2, H=64)
+    for rank in (-1, 4, 1 << 20):
+        assert lib.moe_dispatch_pack_rank(ctypes.byref(d), rank, ok, None, ok, ok, None, ok,
+                                          None) == moe.MOE_ERR_INVALID_ARG
+        assert "outside [0, 4)" in lib.moe_last_error().decode()
+        assert lib.moe_combine_rank(ctypes.byref(d), rank, ok, ok, ok, ok,
+                                    None) == moe.MOE_ERR_INVALID_ARG
+        assert "outside [0, 4)" in lib.moe_last_error().decode()
