@@ -72,8 +72,12 @@ __device__ __forceinline__ int warp_exclusive_scan(int x, int lane) {
 }
 
 // kScales: fp8 rows carry block scales.  A separate instance for the rows
-// without them: the scales loop, even skipped, made the row copy about 20 %
-// slower (GB300, Qwen3-235B-shaped prefill, rank 0: 78 vs 65 us).
+// without them: a scales loop after the row copy, even skipped, made the
+// copy about 20 % slower (GB300, Qwen3-235B-shaped prefill, rank 0: 78 vs
+// 65 us).  With scales, they are copied before the rows, one load per
+// (token, scale) stored to each of the token's rows: on the skewed fp8
+// batch (rank 0: 74,454 rows) 106.5 us, against 124.4 us with the scales
+// loop after the rows and 101 us for the rows alone.
 template <bool kScales>
 __global__ void __launch_bounds__(kPThreads)
 pack_rank_kernel(const uint4 *__restrict__ x, const float *__restrict__ x_scales,
@@ -103,6 +107,13 @@ pack_rank_kernel(const uint4 *__restrict__ x, const float *__restrict__ x_scales
     }
     __syncthreads();
     const int nnz = s_nnz;
+    if (kScales)
+        for (int i = tid; i < nnz * spr; i += kPThreads) {
+            const int q = i / spr, k = i - q * spr;
+            const int t = s_tok[q], n = s_cnt[t];
+            const float sv = __ldg(x_scales + (g0 + t) * spr + k);
+            for (int j = 0; j < n; ++j) packed_scales[(int64_t)s_p[t][j] * spr + k] = sv;
+        }
     const int total = nnz * nvec;  // < 2^31: checked by the launcher
     for (int i0 = tid; i0 < total; i0 += kPThreads * kLU) {
         uint4 v[kLU];
@@ -126,14 +137,6 @@ pack_rank_kernel(const uint4 *__restrict__ x, const float *__restrict__ x_scales
             for (int j = 0; j < n; ++j) packed_x[(int64_t)s_p[t[u]][j] * nvec + c[u]] = v[u];
         }
     }
-    if (kScales)
-        for (int q = 0; q < nnz; ++q) {
-            const int t = s_tok[q], n = s_cnt[t];
-            for (int i = tid; i < n * spr; i += kPThreads) {
-                const int j = i / spr, k = i - j * spr;
-                packed_scales[(int64_t)s_p[t][j] * spr + k] = __ldg(x_scales + (g0 + t) * spr + k);
-            }
-        }
 }
 
 template <int kBf16>
