@@ -13,6 +13,7 @@ import pytest
 
 import oracle
 from combine_moe_route_topk_gb300 import workloads as W
+import sweep_params as S
 from test_parity_gpu import _compare
 
 pytestmark = pytest.mark.gpu
@@ -68,7 +69,7 @@ def _large_shapes(n, seed=77):
     return out
 
 
-SHAPES = _shapes(24) + _large_shapes(6)
+SHAPES = _shapes(S.count(24), S.seed(20261202)) + _large_shapes(S.count(6), S.seed(77))
 
 
 @pytest.mark.parametrize("w", SHAPES, ids=lambda w: w.name)

@@ -19,6 +19,7 @@ import pytest
 import combine_moe_route_topk_gb300 as moe
 from combine_moe_route_topk_gb300 import workloads as W
 from gpu_path import GpuRun
+import sweep_params as S
 from test_pack_quant_gpu import _run as run_quant
 from test_rank_partials_gpu import (check_local_accumulation, check_pack_rank,
                                     check_send_side_partials)
@@ -86,7 +87,7 @@ def _small_fused_shapes(n, seed=33):
     return out
 
 
-@pytest.mark.parametrize("w", _fused_shapes(16) + _small_fused_shapes(12), ids=lambda w: w.name)
+@pytest.mark.parametrize("w", _fused_shapes(S.count(16), S.seed(31)) + _small_fused_shapes(S.count(12), S.seed(33)), ids=lambda w: w.name)
 def test_random_fused_equals_separate_calls(w):
     inp = W.make_inputs(w)
     try:
@@ -120,7 +121,7 @@ def _quant_shapes(n, seed=37):
     return out
 
 
-@pytest.mark.parametrize("w", _quant_shapes(10), ids=lambda w: w.name)
+@pytest.mark.parametrize("w", _quant_shapes(S.count(10), S.seed(37)), ids=lambda w: w.name)
 def test_random_quant_pack(w):
     run_quant(w, W.make_inputs(w))
 
@@ -141,7 +142,7 @@ def _rank_shapes(n, seed=41):
     return out
 
 
-RANK_SHAPES = _rank_shapes(8)
+RANK_SHAPES = _rank_shapes(S.count(8), S.seed(41))
 
 
 @pytest.mark.parametrize("w", RANK_SHAPES, ids=lambda w: w.name)
@@ -173,6 +174,6 @@ def _select_shapes(n, seed=43):
     return out
 
 
-@pytest.mark.parametrize("w", _select_shapes(10), ids=lambda w: w.name)
+@pytest.mark.parametrize("w", _select_shapes(S.count(10), S.seed(43)), ids=lambda w: w.name)
 def test_random_bias_select_route(w):
     _check_route(w, W.make_inputs(w))

@@ -13,8 +13,12 @@ order differently.  The bar:
   order, of the keys recomputed here in fp64 from the raw scores, up to an
   absolute slack of 1e-6 (scores lie in [0, 1], so a few ulp of s plus one
   rounding of a key of magnitude < 4 stays below 5e-7), and its weights are
-  the raw scores of its own selection; such tokens are rare (at most one in
-  a thousand; none on small batches).
+  the raw scores of its own selection.  Such tokens are rare: two selected
+  (or boundary) experts whose raw scores lie within a few ulp of each other,
+  e.g. logits 1.9048145 and 1.9048139 under a softmax over 256 experts, about
+  one token in ten thousand.  Their number is capped at max(2, N*T/1000) only
+  as a guard against a systematic error, which the near-tie check below
+  would catch as well.
 """
 import numpy as np
 import pytest
@@ -63,7 +67,7 @@ def _check_route(w: W.Workload, inp: W.Inputs):
     same = (gi == oi).all(axis=1)
     np.testing.assert_allclose(gw[same], ow[same], rtol=TOPK_W_RTOL, atol=0)
     diff = np.flatnonzero(~same)
-    assert len(diff) <= w.NT // 1000, f"{len(diff)} tokens select differently from the oracle"
+    assert len(diff) <= max(2, w.NT // 1000), f"{len(diff)} tokens select differently from the oracle"
     if len(diff) == 0:
         return
     s64 = _raw_scores64(logits[diff], (w.score_fn & ~FLAG) == W.SOFTMAX)
