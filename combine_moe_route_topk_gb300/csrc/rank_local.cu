@@ -61,16 +61,6 @@ __device__ __forceinline__ void for_pairs_in_window(const int32_t *__restrict__ 
     }
 }
 
-__device__ __forceinline__ int warp_exclusive_scan(int x, int lane) {
-    int incl = x;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += t;
-    }
-    return incl - x;
-}
-
 // kScales: fp8 rows carry block scales.  A separate instance for the rows
 // without them: a scales loop after the row copy, even skipped, made the
 // copy about 20 % slower (GB300, Qwen3-235B-shaped prefill, rank 0: 78 vs
