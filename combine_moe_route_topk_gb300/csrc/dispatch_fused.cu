@@ -36,6 +36,8 @@
 // separate calls).
 #include <mutex>
 
+#include <cuda.h>  // CUcontext and CUresult only: the two driver calls are fetched at run time
+
 #include "mem_ops.cuh"
 #include "moe_internal.cuh"
 #include "route_impl.cuh"
@@ -635,27 +637,72 @@ static __device__ __align__(256) unsigned char g_fused_static_scratch[kStaticScr
 namespace {
 constexpr int kMaxScratchDevices = 64;
 std::mutex g_scratch_mutex;
-void *g_scratch_addr[kMaxScratchDevices] = {};
+
+// The array's address belongs to the CUDA context the library's module was
+// loaded into.  After cudaDeviceReset (or any other end of the primary
+// context) the module is loaded again into a new context, possibly at
+// another address, so the cached address is keyed on the context's unique
+// id as well as on the device.
+struct ScratchEntry {
+    void *addr;
+    unsigned long long ctx_id;
+};
+ScratchEntry g_scratch[kMaxScratchDevices] = {};
+
+// Driver functions fetched through the runtime (no link against libcuda).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+bool g_driver_fns_looked_up = false;
+
+// Unique id of the calling thread's current context; false if there is
+// none yet or the driver cannot say.
+bool current_context_id(unsigned long long *id) {
+    if (!g_driver_fns_looked_up) {
+        g_driver_fns_looked_up = true;
+        cudaDriverEntryPointQueryResult q;
+        void *f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f);
+        cudaGetLastError();
+    }
+    if (g_ctx_get_current == nullptr || g_ctx_get_id == nullptr) return false;
+    CUcontext ctx = nullptr;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return g_ctx_get_id(ctx, id) == CUDA_SUCCESS;
+}
 }  // namespace
 
 int64_t fused_static_scratch_bytes() { return kStaticScratchBytes; }
 
-// Device address of the scratch array on the current device.  In host code
-// the array's name only stands in for it, so the address is looked up once
-// per device (with that device current) and cached.
+// Device address of the scratch array in the current device's context.  In
+// host code the array's name only stands in for it, so the address is
+// looked up with the device current, once per context, and cached.  Where
+// the driver cannot identify the context the lookup is simply repeated on
+// every call.
 cudaError_t fused_static_scratch(void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxScratchDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_addr[dev] == nullptr) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_fused_static_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = p;
+    unsigned long long id = 0;
+    const bool have_id = current_context_id(&id);
+    if (have_id && g_scratch[dev].addr != nullptr && g_scratch[dev].ctx_id == id) {
+        *out = g_scratch[dev].addr;
+        return cudaSuccess;
     }
-    *out = g_scratch_addr[dev];
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_fused_static_scratch);  // creates the context if needed
+    if (e != cudaSuccess) return e;
+    if (current_context_id(&id)) g_scratch[dev] = ScratchEntry{p, id};
+    *out = p;
     return cudaSuccess;
 }
 

@@ -32,6 +32,20 @@
  *     (griddepcontrol.wait / cudaGridDependencySynchronize) before it reads
  *     anything the library writes.  Kernels launched without it, copies and
  *     events are ordered as usual.
+ *
+ * Points where this interface departs from the plain problem statement's
+ * naming, so that a reader can map one onto the other:
+ *   - moe_dispatch_count takes no workspace: it runs in one thread-block
+ *     cluster whose blocks exchange histograms through distributed shared
+ *     memory, so it needs no global scratch.
+ *   - MoeSizes has one field per caller allocation: topk_idx_bytes and
+ *     topk_w_bytes rather than one top-k size; five count-array sizes rather
+ *     than one; total_pairs (N*T*R routed pairs, not rows of a buffer);
+ *     fused_workspace_bytes, the only scratch any call takes.
+ *   - MoeDims.reserved makes the padding before the 64-bit cap_rows explicit
+ *     (the same layout under every compiler and binding); it must be 0.
+ *   - The device status word also reports invalid expert ids
+ *     (MOE_ERR_INVALID_ARG) and bounded waits that gave up (MOE_ERR_TIMEOUT).
  */
 #ifndef MOE_ROUTE_H
 #define MOE_ROUTE_H
@@ -228,7 +242,9 @@ int moe_dispatch_fused(const MoeDims *dims, const float *logits, const float *bi
  *   most 164,288 bytes; larger needs are rejected with MOE_ERR_UNSUPPORTED).
  *   The first call on a device looks up the array's device address (with
  *   that device current); make that first call before any stream capture.
- *   The call itself allocates nothing.
+ *   The address is cached per device and CUDA context: after
+ *   cudaDeviceReset the next call looks it up again, so after a reset, too,
+ *   make one call before capturing.  The call itself allocates nothing.
  *   Every call shares the one array, which keeps the last call's contents;
  *   each call clears the words that must start at zero.  Calls that overlap
  *   on the GPU (other streams, other host threads) race on the array and

@@ -51,8 +51,55 @@ def expert_op_gpu(w: W.Workload, bufs: moe.Buffers, rows: torch.Tensor) -> None:
     raise ValueError(w.expert_op)
 
 
+SENTINEL_BYTE = 0xA5  # packed_x / packed_scales bytes before a pack
+SENTINEL_SRC = -7     # packed_src entries before a pack
+
+
+def fill_sentinels(packed_x: torch.Tensor, packed_scales: torch.Tensor | None,
+                   packed_src: torch.Tensor, rows: torch.Tensor | None = None) -> None:
+    """Set the receive buffers (or only `rows` of them) to the sentinels."""
+    for t in (packed_x, packed_scales):
+        if t is not None:
+            if rows is None:
+                t.view(torch.uint8).fill_(SENTINEL_BYTE)
+            elif rows.numel():
+                t.view(torch.uint8).view(t.shape[0], -1)[rows] = SENTINEL_BYTE
+    if rows is None:
+        packed_src.fill_(SENTINEL_SRC)
+    elif rows.numel():
+        packed_src[rows] = SENTINEL_SRC
+
+
+def _all_bytes_equal(t: torch.Tensor, byte: int) -> bool:
+    """Every byte of t equals `byte` (checked on the device, 1 GB at a time)."""
+    flat = t.reshape(-1).view(torch.uint8)
+    step = 1 << 30
+    for i in range(0, flat.numel(), step):
+        if not bool((flat[i:i + step] == byte).all()):
+            return False
+    return True
+
+
+def assert_untouched_outside(rows: np.ndarray, packed_x: torch.Tensor,
+                             packed_scales: torch.Tensor | None, packed_src: torch.Tensor) -> None:
+    """After the occupied `rows` have been checked: put the sentinels back on
+    them and require every byte of the receive buffers to be a sentinel, i.e.
+    dispatch wrote nothing outside the rows it owns (no stray store into the
+    unused tail of a rank region or past it)."""
+    rt = torch.from_numpy(np.ascontiguousarray(rows, np.int64)).to(packed_x.device)
+    fill_sentinels(packed_x, packed_scales, packed_src, rt)
+    assert _all_bytes_equal(packed_x, SENTINEL_BYTE), "packed_x written outside the occupied rows"
+    if packed_scales is not None:
+        assert _all_bytes_equal(packed_scales, SENTINEL_BYTE), \
+            "packed_scales written outside the occupied rows"
+    assert bool((packed_src == SENTINEL_SRC).all()), "packed_src written outside the occupied rows"
+
+
 class GpuRun:
-    """Route -> count -> pack -> (expert op) -> combine on the current GPU."""
+    """Route -> count -> pack -> (expert op) -> combine on the current GPU.
+
+    The receive buffers start filled with sentinels, so that a test can check
+    that dispatch wrote nothing outside the occupied rows."""
 
     def __init__(self, w: W.Workload, inp: W.Inputs, topk_idx_override: np.ndarray | None = None,
                  fused: bool = False):
@@ -63,6 +110,7 @@ class GpuRun:
                             for t in (inp.logits, inp.bias, inp.x, inp.x_scales)))
         self.bufs = moe.Buffers(self.dims, device=dev)
         b = self.bufs
+        fill_sentinels(b.packed_x, b.packed_scales, b.packed_src)
         if fused:
             assert topk_idx_override is None
             ws = torch.empty(b.sizes["fused_workspace_bytes"], dtype=torch.uint8, device=dev)
@@ -85,6 +133,13 @@ class GpuRun:
                      ("topk_idx", "topk_w", "pos", "expert_counts", "expert_offsets",
                       "rank_counts", "rank_offsets", "send_counts")}
         self.rows = occupied_rows(self.host["rank_counts"], self.cap)
+
+    def assert_untouched_outside_rows(self):
+        """Nothing but the occupied rows of the receive buffers was written.
+        Resets those rows to the sentinels: call after packed_rows(), before
+        combine()."""
+        b = self.bufs
+        assert_untouched_outside(self.rows, b.packed_x, b.packed_scales, b.packed_src)
 
     def packed_rows(self):
         rows = torch.from_numpy(self.rows).to(self.bufs.packed_x.device)
@@ -112,7 +167,7 @@ def check_combine(w: W.Workload, got: torch.Tensor, ref: np.ndarray, mag: np.nda
         lim = BF16_ATOL + BF16_RTOL * np.abs(ref)
     else:
         lim = F32_RTOL_OF_MAG * mag + 1e-30
-    bad = err > lim
+    bad = ~(err <= lim)  # NaN (e.g. an unwritten sentinel) fails too
     if bad.any():
         i = np.argwhere(bad)[0]
         raise AssertionError(f"combine mismatch at {tuple(i)}: got {g[tuple(i)]!r} ref {ref[tuple(i)]!r} "

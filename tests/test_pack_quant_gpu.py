@@ -1,5 +1,6 @@
 """Parity of the quantising pack (bf16 rows -> e4m3 codes + per-128 scales)
-with the oracle: codes, scales and packed_src bit-exact on the occupied rows.
+with the oracle: codes, scales and packed_src bit-exact on the occupied rows,
+and every other byte of the three buffers left as it was (sentinels).
 
 Both sides take every rounding decision in the same precision: amax is exact,
 scale = fl32(amax / 448), the quotient fl32(x / scale) is IEEE-rounded on
@@ -13,7 +14,7 @@ import torch
 import combine_moe_route_topk_gb300 as moe
 import oracle
 from combine_moe_route_topk_gb300 import workloads as W
-from gpu_path import compact_of_region, occupied_rows
+from gpu_path import assert_untouched_outside, compact_of_region, fill_sentinels, occupied_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -37,6 +38,9 @@ def _run(w, inp, special=None):
     moe.route_topk(dims, logits, bias, w.score_fn, w.renormalize, b.topk_idx, b.topk_w)
     moe.dispatch_count(dims, b.topk_idx, b.expert_counts, b.expert_offsets, b.rank_counts,
                        b.rank_offsets, b.send_counts, b.pos, b.status)
+    pq2 = packed_q.view(-1, w.H)
+    ps2 = packed_scales.view(-1, w.H // 128)
+    fill_sentinels(pq2, ps2, b.packed_src)
     moe.dispatch_pack_quant(dims, x, b.pos, packed_q, packed_scales, b.packed_src)
     assert moe.read_status(b.status) == moe.MOE_OK
     cap = b.sizes["cap_rows"]
@@ -59,6 +63,8 @@ def _run(w, inp, special=None):
     bad = np.argwhere(gq != oq[crow])
     assert bad.size == 0, (f"{len(bad)} codes differ, first at {tuple(bad[0])}: "
                            f"got {gq[tuple(bad[0])]:#04x} want {oq[crow][tuple(bad[0])]:#04x}")
+    # nothing outside the occupied rows was written
+    assert_untouched_outside(rows, pq2, ps2, b.packed_src)
 
 
 def test_quant_pack_full_size_dsv3():

@@ -41,6 +41,21 @@ def _oracle_route_count(w, inp):
     return idx, tw, cnt, st
 
 
+def restore_packed_rows(gr, gpx, gps, gsrc):
+    """Put the packed rows the GPU wrote (copied out by packed_rows() and
+    already checked) back after the sentinel check, for the expert op and
+    combine."""
+    b = gr.bufs
+    if gr.rows.size == 0:
+        return
+    dev = b.packed_x.device
+    rt = torch.from_numpy(gr.rows).to(dev)
+    b.packed_x.view(torch.uint8).view(b.packed_x.shape[0], -1)[rt] = torch.from_numpy(gpx).to(dev)
+    b.packed_src[rt] = torch.from_numpy(gsrc).to(dev)
+    if gps is not None:
+        b.packed_scales[rt] = torch.from_numpy(gps).to(dev)
+
+
 def _compare(w, inp, topk_idx_override=None, combine_tokens=None, fused=False):
     gr = GpuRun(w, inp, topk_idx_override=topk_idx_override, fused=fused)
     h = gr.host
@@ -69,7 +84,11 @@ def _compare(w, inp, topk_idx_override=None, combine_tokens=None, fused=False):
     np.testing.assert_array_equal(gpx, opx[crow])
     if ops is not None:
         np.testing.assert_array_equal(gps, ops[crow])
-    # combine
+    # and nothing else: every other byte of the receive buffers still holds
+    # its sentinel (this puts the sentinels back on the occupied rows too)
+    gr.assert_untouched_outside_rows()
+    # combine (y is recomputed from packed rows, so put them back first)
+    restore_packed_rows(gr, gpx, gps, gsrc)
     out = gr.combine()
     y = oracle.expert_op(w.expert_op, opx, ops, osrc, idx, w.H, w.x_dtype, w.y_dtype)
     pos, wt = cnt["pos"], tw

@@ -7,11 +7,15 @@ cudaMalloc on its hot path (it synchronises the device and can fail under
 memory pressure).  For them moe_dispatch_fused_static runs the fused
 route + count + pack with scratch that lives in the library itself.
 
-The GPU test calls it through the C ABI twice in a row, on two different
-batches, and checks every output of each call against moe_dispatch_fused
-given a freshly allocated workspace.  The second call sees the scratch as
-the first call left it, so anything that must start at zero and was not
-cleared would show up there.  Integer outputs and packed rows must be equal
+The GPU test calls it through the C ABI several times in a row, on batches
+of different shapes, and then checks every output of each call against
+moe_dispatch_fused given a freshly allocated (uninitialised) workspace.
+The calls shrink from the widest scratch use to a narrower one: 512
+experts and 16 counting blocks, then 256 experts and 16 blocks, then 96
+experts, 4 ranks and 3 blocks.  Each later call sees the scratch as the
+previous one left it, including histogram and staging words past its own
+experts, ranks and blocks, so a call that read anything it had not written
+or cleared first would show up there.  Integer outputs and packed rows must be equal
 byte for byte; router weights within the relative 2e-6 that the other
 parity tests allow (both calls run the same kernel, so they agree exactly
 in practice).
@@ -19,8 +23,6 @@ in practice).
 This file sorts last so that a run stopping at its first failure has run
 every other test before it.
 """
-import dataclasses
-
 import numpy as np
 import pytest
 import torch
@@ -52,25 +54,39 @@ def _dispatch(w: W.Workload, d: W.Inputs, static: bool) -> dict:
             for k in OUTPUTS}
 
 
+# cooperative-kernel batches (more than 512 tokens, T % 32 == 0, R <= 8),
+# widest scratch use first.  Receive regions of 4096 rows per rank (the
+# largest rank receives 2774, 1945 and 1001 rows) keep the buffers compared
+# on the host small; the capacity does not change what the scratch holds.
+STATIC_SEQUENCE = (
+    W.Workload("e512", N=16, T=256, E=512, R=8, H=1024, score_fn=W.SIGMOID, bias="normal",
+               renormalize=True, cap_rows=4096, seed=301),
+    W.WORKLOADS["dsv3_decode"].replace(seed=302, cap_rows=4096),
+    W.Workload("e96", N=4, T=160, E=96, R=6, H=2048, renormalize=True, cap_rows=4096, seed=303),
+)
+
+
 @pytest.mark.gpu
-def test_static_scratch_matches_allocated_workspace_on_two_calls_in_a_row():
+def test_static_scratch_matches_allocated_workspace_on_calls_in_a_row():
     from combine_moe_route_topk_gb300 import _build
     _build.build()
     dev = torch.device("cuda", torch.cuda.current_device())
-    base = W.WORKLOADS["dsv3_decode"]
-    for seed in (base.seed + 101, base.seed + 202):
-        w = dataclasses.replace(base, seed=seed)
+    inputs = []
+    for w in STATIC_SEQUENCE:
         inp = W.make_inputs(w)
-        d = W.Inputs(*(t.to(dev) if t is not None else None
-                       for t in (inp.logits, inp.bias, inp.x, inp.x_scales)))
-        got = _dispatch(w, d, static=True)
+        inputs.append(W.Inputs(*(t.to(dev) if t is not None else None
+                                 for t in (inp.logits, inp.bias, inp.x, inp.x_scales))))
+    # the static calls back to back, then the same batches with a workspace
+    got = [_dispatch(w, d, static=True) for w, d in zip(STATIC_SEQUENCE, inputs)]
+    for w, d, g in zip(STATIC_SEQUENCE, inputs, got):
         want = _dispatch(w, d, static=False)
-        assert int(want["status"][0]) == moe.MOE_OK
+        assert int(want["status"][0]) == moe.MOE_OK, w.name
         for k in OUTPUTS:
             if k == "topk_w":
-                np.testing.assert_allclose(got[k], want[k], rtol=TOPK_W_RTOL, atol=0, err_msg=k)
+                np.testing.assert_allclose(g[k], want[k], rtol=TOPK_W_RTOL, atol=0,
+                                           err_msg=f"{k} ({w.name})")
             else:
-                np.testing.assert_array_equal(got[k], want[k], err_msg=f"{k} (seed {seed})")
+                np.testing.assert_array_equal(g[k], want[k], err_msg=f"{k} ({w.name})")
 
 
 def test_static_variant_rejects_shapes_the_fused_kernel_cannot_take():
