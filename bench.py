@@ -49,6 +49,16 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="CPU work for the oracle baseline (0 disables it)")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--tokens-per-rank", type=int, default=0,
+                   help="T of the workload (0: its own); a smaller batch of the same shape, for "
+                        "profiling captures that must stay small")
+    p.add_argument("--no-extras", action="store_true",
+                   help="time the step and its breakdown only (no graphs, variants, end-to-end "
+                        "run or other workloads)")
+    p.add_argument("--no-other-workloads", dest="other_workloads", action="store_false",
+                   help="leave out the table of the other workloads")
+    p.add_argument("--workload-steps", type=int, default=100,
+                   help="timed steps per workload of the workloads table")
     p.add_argument("--cap-rows", type=int, default=0,
                    help="per-rank receive capacity (0: the bound N*T*max(R,E/N)); a smaller "
                         "capacity shrinks the allocation, not the work")
@@ -298,6 +308,286 @@ def workload_config(w):
 # GPU arm
 # --------------------------------------------------------------------------
 
+def new_events(n):
+    import torch
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def mean_interval(pairs):
+    return statistics.mean(a.elapsed_time(b) for a, b in pairs)
+
+
+class PathRunner:
+    """One workload on one GPU: its seeded inputs in HBM, its buffers, and the
+    four calls of the path.  The expert op between pack and combine stands in
+    for the grouped expert GEMM and is not run: combine reads y as pack left
+    it (identity) or as it was zeroed once (a separate y)."""
+
+    def __init__(self, moe, W, w, dev, stream, flush):
+        self.moe, self.w, self.dev, self.stream, self.flush = moe, w, dev, stream, flush
+        self.dims = moe.dims_of(w)
+        self.inp_cpu = W.make_inputs(w)
+        self.inp = W.Inputs(*(t.to(dev) if t is not None else None
+                              for t in (self.inp_cpu.logits, self.inp_cpu.bias, self.inp_cpu.x,
+                                        self.inp_cpu.x_scales)))
+        self.b = moe.Buffers(self.dims, device=dev,
+                             separate_y=False if w.x_dtype == w.y_dtype else None)
+        if self.b.y.data_ptr() != self.b.packed_x.data_ptr():
+            self.b.y.zero_()
+
+    def launch(self, k, s=None):
+        moe, w, b, inp, dims = self.moe, self.w, self.b, self.inp, self.dims
+        s = self.stream if s is None else s
+        if k == "route":
+            moe.route_topk(dims, inp.logits, inp.bias, w.score_fn, w.renormalize, b.topk_idx,
+                           b.topk_w, s)
+        elif k == "count":
+            moe.dispatch_count(dims, b.topk_idx, b.expert_counts, b.expert_offsets,
+                               b.rank_counts, b.rank_offsets, b.send_counts, b.pos, b.status, s)
+        elif k == "pack":
+            moe.dispatch_pack(dims, inp.x, inp.x_scales, b.pos, b.packed_x, b.packed_scales,
+                              b.packed_src, s)
+        else:
+            moe.combine(dims, b.y, b.pos, b.topk_w, b.out, s)
+
+    def step(self, ev):
+        """dispatch (route -> count -> pack back to back, so each launch
+        overlaps the tail of the previous kernel), the expert-op stand-in (an
+        L2 flush, untimed), combine, and the L2 flush before the next step.
+        Events: [0] dispatch [1] flush [2] combine [3] flush [4]."""
+        st = self.stream
+        ev[0].record(st)
+        self.launch("route")
+        self.launch("count")
+        self.launch("pack")
+        ev[1].record(st)
+        self.flush()
+        ev[2].record(st)
+        self.launch("combine")
+        ev[3].record(st)
+        self.flush()
+        ev[4].record(st)
+
+    def check_status(self):
+        st = self.moe.read_status(self.b.status, self.stream)
+        if st != self.moe.MOE_OK:
+            raise SystemExit(f"dispatch_count status {self.moe.STATUS_NAMES.get(st, st)} on {self.w.name}")
+
+    def steps(self, n):
+        """n steps, each self-contained (it ends with the flush the next one
+        starts after).  Returns the per-step events."""
+        evs = [new_events(5) for _ in range(n)]
+        for e in evs:
+            self.step(e)
+        return evs
+
+    def clean_flush_ms(self, n):
+        """An L2 flush on an L2 that holds only clean lines (the previous
+        flush's): the baseline that the flushes inside a step are compared
+        with, to charge the write-back of the dirty lines a kernel left."""
+        pool = [new_events(2) for _ in range(n)]
+        self.flush()
+        for e in pool:
+            e[0].record(self.stream)
+            self.flush()
+            e[1].record(self.stream)
+        import torch
+        torch.cuda.synchronize(self.dev)
+        return mean_interval(pool)
+
+    def breakdown(self, n, host_lead):
+        """Per-kernel times: an event between every two kernels (the events
+        serialise the launches, so these sum to a little more than a step);
+        and route -> count back to back, what the dispatch segment spends
+        before pack's own work."""
+        import torch
+        st = self.stream
+        pool = [new_events(6) for _ in range(n)]
+        host_lead(n)
+        for ev in pool:
+            self.flush()
+            ev[0].record(st)
+            for i, k in enumerate(("route", "count", "pack")):
+                self.launch(k)
+                ev[i + 1].record(st)
+            self.flush()
+            ev[4].record(st)
+            self.launch("combine")
+            ev[5].record(st)
+        rc = [new_events(2) for _ in range(n)]
+        host_lead(n)
+        for e in rc:
+            self.flush()
+            e[0].record(st)
+            self.launch("route")
+            self.launch("count")
+            e[1].record(st)
+        torch.cuda.synchronize(self.dev)
+        per = {"route": [e[0].elapsed_time(e[1]) for e in pool],
+               "count": [e[1].elapsed_time(e[2]) for e in pool],
+               "pack": [e[2].elapsed_time(e[3]) for e in pool],
+               "combine": [e[4].elapsed_time(e[5]) for e in pool]}
+        return per, mean_interval(rc)
+
+    def timed_repeat(self, fn, n, host_lead):
+        """Mean event time of fn() run alone after an L2 flush, n times."""
+        import torch
+        pool = [new_events(2) for _ in range(n + 3)]
+        host_lead(n + 3)
+        for e in pool:
+            self.flush()
+            e[0].record(self.stream)
+            fn()
+            e[1].record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        return mean_interval(pool[3:])
+
+    def fused_ms(self, n, host_lead):
+        """moe_dispatch_fused on the same batch, or why it does not take it."""
+        import torch
+        moe, w, b, inp, dims = self.moe, self.w, self.b, self.inp, self.dims
+        try:
+            ws = torch.empty(moe.buffer_sizes(dims)["fused_workspace_bytes"], dtype=torch.uint8,
+                             device=self.dev)
+
+            def call():
+                moe.dispatch_fused(dims, inp.logits, inp.bias, w.score_fn, w.renormalize, inp.x,
+                                   inp.x_scales, b.topk_idx, b.topk_w, b.expert_counts,
+                                   b.expert_offsets, b.rank_counts, b.rank_offsets,
+                                   b.send_counts, b.pos, b.status, b.packed_x, b.packed_scales,
+                                   b.packed_src, ws, self.stream)
+            ms = self.timed_repeat(call, n, host_lead)
+            if moe.read_status(b.status, self.stream) != moe.MOE_OK:
+                raise RuntimeError("fused dispatch status")
+            return {"ms": ms}
+        except moe.MoeError as ex:
+            return {"unsupported": str(ex)}
+
+    def ep_local(self, n, host_lead, rank=0):
+        """The expert-parallel local path of one rank: rank-restricted pack,
+        then (after an L2 flush) its local accumulation; events around each."""
+        import torch
+        moe, w, b, inp, dims = self.moe, self.w, self.b, self.inp, self.dims
+        from combine_moe_route_topk_gb300 import workloads as W
+        # the default routing in place
+        self.launch("route")
+        self.launch("count")
+        self.launch("pack")
+        torch.cuda.synchronize(self.dev)
+        cap = moe.buffer_sizes(dims)["cap_rows"]
+        rows = int(b.rank_counts[rank].item())
+        toks = int(((b.pos >= rank * cap) & (b.pos < (rank + 1) * cap)).any(dim=1).sum().item())
+        out2 = torch.empty_like(b.out)
+        pool = [(new_events(2), new_events(2)) for _ in range(n + 3)]
+        host_lead(n + 3)
+        for e, e2 in pool:
+            self.flush()
+            e[0].record(self.stream)
+            moe.dispatch_pack_rank(dims, rank, inp.x, inp.x_scales, b.pos, b.packed_x,
+                                   b.packed_scales, b.packed_src, self.stream)
+            e[1].record(self.stream)
+            self.flush()
+            e2[0].record(self.stream)
+            moe.combine_rank(dims, rank, b.y, b.pos, b.topk_w, out2, self.stream)
+            e2[1].record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        t_pr = mean_interval([e for e, _ in pool[3:]])
+        t_cr = mean_interval([e2 for _, e2 in pool[3:]])
+        del out2
+        rb, yb = W.row_bytes(w), W.y_row_bytes(w)
+        sb = 4 * (w.H // 128) if w.x_dtype == W.FP8E4M3_BLK128 else 0
+        b_pr = toks * (rb + sb) + rows * (rb + sb) + rows * 4 + w.NT * w.R * 4
+        b_cr = rows * yb + w.NT * yb + w.NT * w.R * 8
+        peak = measured_peaks()[0]
+        return {"rank": rank, "rows": rows, "tokens": toks,
+                "pack_rank_ms": t_pr, "pack_rank_alg_bytes": b_pr,
+                "pack_rank_alg_gbs": b_pr / (t_pr / 1e3) / 1e9,
+                "pack_rank_frac": b_pr / (t_pr / 1e3) / 1e9 / peak,
+                "combine_rank_ms": t_cr, "combine_rank_alg_bytes": b_cr,
+                "combine_rank_alg_gbs": b_cr / (t_cr / 1e3) / 1e9,
+                "combine_rank_frac": b_cr / (t_cr / 1e3) / 1e9 / peak}
+
+    def free(self):
+        del self.b, self.inp
+
+
+def roofline_of(w, kern, launch_ms, writeback_ms, peak, peak_kind):
+    """Roofline entry of the dominant kernel (the slower of pack and combine by
+    median): algorithmic bytes over its mean event time; the DRAM-level
+    fraction from the committed ncu traffic of the same source; and the
+    fraction with the write-back of its dirty L2 lines charged to it."""
+    from combine_moe_route_topk_gb300 import workloads as W
+    alg = W.algorithmic_bytes(w)
+    dom = max(("pack", "combine"), key=lambda k: kern[k]["median_ms"])
+    ms = launch_ms[dom]
+    achieved = alg[dom] / (ms / 1e3) / 1e9
+    traffic = ncu_traffic(dom, w.name)
+    wb = max(0.0, writeback_ms[dom])
+    r = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+         "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+         if peak_kind == "measured" else "fallback 6.8 TB/s",
+         "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+         "frac_dram": None if traffic is None else traffic / (ms / 1e3) / 1e9 / peak,
+         "frac_with_writeback": alg[dom] / ((ms + wb) / 1e3) / 1e9 / peak,
+         "alg_bytes_per_launch": alg[dom], "launch_ms": ms, "writeback_ms": wb}
+    return r
+
+
+def measure_workload(runner, steps, nb, host_lead, sampler_window=None):
+    """The step, its per-kernel breakdown, the write-back of the dirty lines
+    pack and combine leave in L2, and the fused and expert-parallel local
+    variants, for one workload: the entry of the `workloads` table."""
+    import torch
+    w = runner.w
+    from combine_moe_route_topk_gb300 import workloads as W
+    runner.flush()
+    runner.steps(3)
+    runner.check_status()
+    torch.cuda.synchronize(runner.dev)
+    host_lead(steps)
+    evs = runner.steps(steps)
+    torch.cuda.synchronize(runner.dev)
+    runner.check_status()
+    disp = [e[0].elapsed_time(e[1]) for e in evs]
+    comb = [e[2].elapsed_time(e[3]) for e in evs]
+    fl_p = [e[1].elapsed_time(e[2]) for e in evs]
+    fl_c = [e[3].elapsed_time(e[4]) for e in evs]
+    clean = runner.clean_flush_ms(nb)
+    per, rc_ms = runner.breakdown(nb, host_lead)
+    alg = W.algorithmic_bytes(w)
+    peak, peak_kind = measured_peaks()
+    kern = {k: {"ms": statistics.mean(v), "median_ms": statistics.median(v),
+                "alg_gbs": alg[k] / (statistics.mean(v) / 1e3) / 1e9} for k, v in per.items()}
+    step_ms = statistics.mean(a + c for a, c in zip(disp, comb))
+    wb = {"pack": statistics.mean(fl_p) - clean, "combine": statistics.mean(fl_c) - clean}
+    launch_ms = {"pack": kern["pack"]["ms"], "combine": statistics.mean(comb)}
+    pc_ms = launch_ms["pack"] + launch_ms["combine"]
+    pc_gbs = (alg["pack"] + alg["combine"]) / (pc_ms / 1e3) / 1e9
+    pc_wb_ms = pc_ms + max(0.0, wb["pack"]) + max(0.0, wb["combine"])
+    pc_wb_gbs = (alg["pack"] + alg["combine"]) / (pc_wb_ms / 1e3) / 1e9
+    entry = {
+        "config": {"N": w.N, "T": w.T, "tokens": w.NT, "E": w.E, "R": w.R, "H": w.H,
+                   "x_dtype": {0: "bf16", 1: "f32", 2: "fp8e4m3+f32/128"}[w.x_dtype]},
+        "steps": steps, "ms_per_step": step_ms, "tokens_per_s": w.NT / (step_ms / 1e3),
+        "dispatch_ms": statistics.mean(disp), "combine_ms": statistics.mean(comb),
+        "route_count_chain_ms": rc_ms,
+        "kernels": kern,
+        "pack_plus_combine": {"ms": pc_ms, "alg_gbs": pc_gbs, "frac": pc_gbs / peak,
+                              "ms_with_writeback": pc_wb_ms,
+                              "frac_with_writeback": pc_wb_gbs / peak},
+        "writeback_ms": {"after_pack": wb["pack"], "after_combine": wb["combine"],
+                         "clean_flush_ms": clean,
+                         "note": "L2 flush right after the kernel minus a flush of an L2 "
+                                 "holding only clean lines: the write-back of the dirty "
+                                 "lines the kernel left, which the step does not time"},
+        "step_with_writeback_ms": step_ms + max(0.0, wb["pack"]) + max(0.0, wb["combine"]),
+        "roofline": roofline_of(w, kern, launch_ms, wb, peak, peak_kind),
+    }
+    entry["fused_dispatch"] = runner.fused_ms(nb, host_lead)
+    entry["ep_local_rank0"] = runner.ep_local(nb, host_lead)
+    return entry, (disp, comb, fl_p, fl_c, clean, per, rc_ms)
+
+
 def run_ours(args):
     import torch
     import combine_moe_route_topk_gb300 as moe
@@ -316,13 +606,10 @@ def run_ours(args):
     moe.lib()  # fails loudly if the library was not built
 
     w = W.WORKLOADS[args.workload]
+    if args.tokens_per_rank:
+        w = w.replace(T=args.tokens_per_rank)
     if args.cap_rows:
         w = w.replace(cap_rows=args.cap_rows)
-    dims = moe.dims_of(w)
-    inp_cpu = W.make_inputs(w)
-    inp = W.Inputs(*(t.to(dev) if t is not None else None
-                     for t in (inp_cpu.logits, inp_cpu.bias, inp_cpu.x, inp_cpu.x_scales)))
-    b = moe.Buffers(dims, device=dev, separate_y=False if w.x_dtype == w.y_dtype else None)
     stream = torch.cuda.current_stream(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     # L2 flush: read a buffer twice the L2 size.  Every line a step left in
@@ -335,49 +622,6 @@ def run_ours(args):
     def flush():
         torch.sum(flush_buf, dim=0, out=flush_out)
 
-    def launch(k, s=None):
-        s = stream if s is None else s
-        if k == "route":
-            moe.route_topk(dims, inp.logits, inp.bias, w.score_fn, w.renormalize, b.topk_idx,
-                           b.topk_w, s)
-        elif k == "count":
-            moe.dispatch_count(dims, b.topk_idx, b.expert_counts, b.expert_offsets,
-                               b.rank_counts, b.rank_offsets, b.send_counts, b.pos, b.status, s)
-        elif k == "pack":
-            moe.dispatch_pack(dims, inp.x, inp.x_scales, b.pos, b.packed_x, b.packed_scales,
-                              b.packed_src, s)
-        else:
-            moe.combine(dims, b.y, b.pos, b.topk_w, b.out, s)
-
-    def step(ev):
-        # dispatch (route -> count -> pack) back to back, so each kernel's
-        # launch overlaps the tail of the previous one; then the expert-op
-        # stand-in (L2 flush, untimed); then combine.
-        ev[0].record(stream)
-        launch("route")
-        launch("count")
-        launch("pack")
-        ev[1].record(stream)
-        flush()
-        ev[2].record(stream)
-        launch("combine")
-        ev[3].record(stream)
-
-    def step_breakdown(ev):
-        # one event between every two kernels: per-kernel times (the events
-        # serialise the launches, so these sum to a little more than a step)
-        ev[0].record(stream)
-        for i, k in enumerate(("route", "count", "pack")):
-            launch(k)
-            ev[i + 1].record(stream)
-        flush()
-        ev[4].record(stream)
-        launch("combine")
-        ev[5].record(stream)
-
-    def new_events(n=6):
-        return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-
     def host_lead(iters):
         # The loops after the timed region bracket single short kernels with
         # events, and Python needs tens of microseconds per call: a GPU sleep
@@ -387,24 +631,24 @@ def run_ours(args):
         if sleep is not None:
             sleep(int(iters * 150e-6 * 2.0e9))
 
-    for _ in range(max(3, args.warmup)):
-        flush()
-        step(new_events(4))
-    st = moe.read_status(b.status, stream)
-    if st != moe.MOE_OK:
-        raise SystemExit(f"dispatch_count status {moe.STATUS_NAMES.get(st, st)} on {w.name}")
+    run = PathRunner(moe, W, w, dev, stream, flush)
+    dims, b, inp, inp_cpu = run.dims, run.b, run.inp, run.inp_cpu
+    launch = run.launch
+
+    flush()
+    run.steps(max(3, args.warmup))
+    run.check_status()
 
     sampler = None if args.no_clocks else ClockSampler(local_rank)
     if sampler is not None:
         sampler.wait_first()
-    evs = [new_events(4) for _ in range(args.steps)]
+    evs = [new_events(5) for _ in range(args.steps)]
     if pg:
         pg.barrier()
     torch.cuda.synchronize(dev)
     t_wall0 = time.time()
-    for i in range(args.steps):
-        flush()
-        step(evs[i])
+    for e in evs:
+        run.step(e)
     torch.cuda.synchronize(dev)
     if pg:
         pg.barrier()
@@ -414,54 +658,131 @@ def run_ours(args):
         time.sleep(0.05)
         sampler.stop()
         clocks = sampler.summary(t_wall0, t_wall1)
+    run.check_status()
 
-    dispatch_ms = [ev[0].elapsed_time(ev[1]) for ev in evs]
-    combine_ms = [ev[2].elapsed_time(ev[3]) for ev in evs]
+    dispatch_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    combine_ms = [e[2].elapsed_time(e[3]) for e in evs]
     step_ms = [a + c for a, c in zip(dispatch_ms, combine_ms)]
     ms = reduce_max(statistics.mean(step_ms), pg)
     value = job_throughput(w.NT, world, ms)
+    fl_pack = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    fl_comb = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
 
-    # per-kernel breakdown, after the timed region
+    # ---- after the timed region: breakdown, write-back, variants ---------
     nb = max(10, min(args.steps, 200))
-    bevs = [new_events(6) for _ in range(nb)]
-    host_lead(nb)
-    for i in range(nb):
-        flush()
-        step_breakdown(bevs[i])
-    torch.cuda.synchronize(dev)
-    # route -> count back to back (with PDL, as in the step): what the
-    # dispatch segment spends before pack's own work
-    rcpool = [new_events(2) for _ in range(nb)]
-    host_lead(nb)
-    for i in range(nb):
-        flush()
-        rcpool[i][0].record(stream)
-        launch("route")
-        launch("count")
-        rcpool[i][1].record(stream)
-    torch.cuda.synchronize(dev)
-    route_count_chain_ms = statistics.mean(a.elapsed_time(c) for a, c in rcpool)
-    per = {k: [] for k in KERNELS}
-    for ev in bevs:
-        per["route"].append(ev[0].elapsed_time(ev[1]))
-        per["count"].append(ev[1].elapsed_time(ev[2]))
-        per["pack"].append(ev[2].elapsed_time(ev[3]))
-        per["combine"].append(ev[4].elapsed_time(ev[5]))
+    clean = run.clean_flush_ms(nb)
+    wb = {"pack": fl_pack - clean, "combine": fl_comb - clean}
+    per, route_count_chain_ms = run.breakdown(nb, host_lead)
     per_timed = {"dispatch (route+count+pack)": statistics.mean(dispatch_ms),
                  "combine": statistics.mean(combine_ms),
                  "route+count alone, back to back (diagnostic)": route_count_chain_ms}
+    step_wb_ms = reduce_max(statistics.mean(step_ms) + max(0.0, wb["pack"]) + max(0.0, wb["combine"]), pg)
 
-    # the same step replayed from CUDA graphs, as a serving loop runs it:
-    # dispatch (route -> count -> pack, with their programmatic-dependency
-    # edges) and combine captured once each, the L2 flush between replays
+    graph_replay = extra = e2e = None
+    if not args.no_extras:
+        graph_replay = graph_replay_of(args, run, host_lead, pg, world)
+        extra = variants_of(args, run, nb, host_lead, per_timed)
+        e2e = run_e2e(args, w, dims, inp_cpu, b, dev, stream, flush, moe)
+
+    alg = W.algorithmic_bytes(w)
+    peak, peak_kind = measured_peaks()
+    kern = {}
+    for k in KERNELS:
+        mean_ms = statistics.mean(per[k])
+        kern[k] = {"ms": mean_ms, "median_ms": statistics.median(per[k]),
+                   "alg_bytes": alg[k], "alg_gbs": alg[k] / (mean_ms / 1e3) / 1e9}
+    # combine has its own events inside the timed region; pack's come from
+    # the breakdown pass right after it
+    launch_ms = {"pack": kern["pack"]["ms"], "combine": per_timed["combine"]}
+    roofline = roofline_of(w, kern, launch_ms, wb, peak, peak_kind)
+    pc_ms = launch_ms["pack"] + launch_ms["combine"]
+    pc_gbs = (alg["pack"] + alg["combine"]) / (pc_ms / 1e3) / 1e9
+    pc_wb_ms = pc_ms + max(0.0, wb["pack"]) + max(0.0, wb["combine"])
+    pc_wb_gbs = (alg["pack"] + alg["combine"]) / (pc_wb_ms / 1e3) / 1e9
+
+    # ---- the other workloads, each on its own buffers ---------------------
+    workloads = None
+    if not args.no_extras and args.other_workloads:
+        run.free()
+        del run, b, inp
+        torch.cuda.empty_cache()
+        workloads = {}
+        wsampler = None if args.no_clocks else ClockSampler(local_rank)
+        if wsampler is not None:
+            wsampler.wait_first()
+        tw0 = time.time()
+        for name in W.WORKLOADS:
+            if name == w.name:
+                continue
+            r2 = PathRunner(moe, W, W.WORKLOADS[name], dev, stream, flush)
+            entry, _ = measure_workload(r2, args.workload_steps, max(10, min(args.workload_steps, 50)),
+                                        host_lead)
+            workloads[name] = entry
+            r2.free()
+            del r2
+            torch.cuda.empty_cache()
+        if wsampler is not None:
+            time.sleep(0.05)
+            wsampler.stop()
+            workloads["clocks"] = wsampler.summary(tw0, time.time())
+
+    if rank != 0:
+        return 0
+    cpu = None
+    if world == 1 and args.cpu_seconds > 0:
+        import oracle
+        oracle.build_lib()
+        cpu = cpu_baseline(w, inp_cpu, args.cpu_seconds)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "io_dtype": "bf16", "data": "synthetic", "config": workload_config(w),
+        "gpu_launches": 4 * args.steps,
+        "roofline": roofline,
+        "pack_plus_combine": {"ms": pc_ms, "alg_gbs": pc_gbs, "frac": pc_gbs / peak,
+                              "frac_of_8tbs_nominal": pc_gbs / 8000.0,
+                              "ms_with_writeback": pc_wb_ms,
+                              "frac_with_writeback": pc_wb_gbs / peak},
+        "step_with_writeback_ms": step_wb_ms,
+        "writeback_ms": {"after_pack": wb["pack"], "after_combine": wb["combine"],
+                         "clean_flush_ms": clean,
+                         "note": "the L2 flush that follows pack (and combine) inside every "
+                                 "step, minus a flush of an L2 holding only clean lines: the "
+                                 "write-back of the dirty lines the kernel left in L2, which "
+                                 "the timed segments do not include; step_with_writeback_ms "
+                                 "charges it"},
+        "timed_segments_ms": per_timed,
+        "graph_replay": graph_replay,
+        "kernels": kern,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "wall_s_timed_region": t_wall1 - t_wall0,
+    }
+    if extra is not None:
+        line.update(extra)
+    if workloads is not None:
+        line["workloads"] = workloads
+    print(json.dumps(line))
+    return 0
+
+
+def graph_replay_of(args, run, host_lead, pg, world):
+    """The same step replayed from CUDA graphs, as a serving loop runs it:
+    dispatch (route -> count -> pack, with their programmatic-dependency
+    edges) and combine captured once each, the L2 flush between replays."""
+    import torch
+    dev, stream, flush = run.dev, run.stream, run.flush
     cap_stream = torch.cuda.Stream(dev)
     g_disp, g_comb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     cap_stream.wait_stream(stream)
     with torch.cuda.graph(g_disp, stream=cap_stream):
         for k in ("route", "count", "pack"):
-            launch(k, cap_stream)
+            run.launch(k, cap_stream)
     with torch.cuda.graph(g_comb, stream=cap_stream):
-        launch("combine", cap_stream)
+        run.launch("combine", cap_stream)
     stream.wait_stream(cap_stream)
     n_g = args.steps + max(3, args.warmup)
     gpool = [new_events(4) for _ in range(n_g)]
@@ -480,16 +801,25 @@ def run_ours(args):
         if i >= max(3, args.warmup):
             gevs.append(e)
     torch.cuda.synchronize(dev)
-    if moe.read_status(b.status, stream) != moe.MOE_OK:
-        raise SystemExit("dispatch_count status after graph replays")
+    run.check_status()
     g_step = [e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in gevs]
     g_ms = reduce_max(statistics.mean(g_step), pg)
-    graph_replay = {"ms_per_step": g_ms, "median_ms_per_step": statistics.median(g_step),
-                    "dispatch_ms": statistics.mean(e[0].elapsed_time(e[1]) for e in gevs),
-                    "combine_ms": statistics.mean(e[2].elapsed_time(e[3]) for e in gevs),
-                    "value": job_throughput(w.NT, world, g_ms), "replays": len(gevs),
-                    "note": "two CUDA graphs (dispatch, combine) replayed per step"}
     del g_disp, g_comb
+    return {"ms_per_step": g_ms, "median_ms_per_step": statistics.median(g_step),
+            "dispatch_ms": statistics.mean(e[0].elapsed_time(e[1]) for e in gevs),
+            "combine_ms": statistics.mean(e[2].elapsed_time(e[3]) for e in gevs),
+            "value": job_throughput(run.w.NT, world, g_ms), "replays": len(gevs),
+            "note": "two CUDA graphs (dispatch, combine) replayed per step"}
+
+
+def variants_of(args, run, nb, host_lead, per_timed):
+    """The quantising pack, the decode-fused dispatch, the bias-for-selection
+    router, the send-side combine and the expert-parallel local path, each on
+    the headline batch."""
+    import torch
+    moe, w, b, inp, dims, dev, stream = run.moe, run.w, run.b, run.inp, run.dims, run.dev, run.stream
+    from combine_moe_route_topk_gb300 import workloads as W
+    out = {}
 
     # the quantising pack (bf16 rows -> e4m3 + per-128 scales), timed alone
     # on the same routing; it replaces pack when the experts take fp8 input
@@ -498,34 +828,16 @@ def run_ours(args):
         qs = moe.buffer_sizes(moe.fp8_dims(dims))
         pq = torch.empty(qs["packed_x_bytes"], dtype=torch.uint8, device=dev)
         ps = torch.empty(qs["packed_scales_bytes"] // 4, dtype=torch.float32, device=dev)
-        qms = []
-        qpool = [new_events(2) for _ in range(nb + 3)]
-        host_lead(nb + 3)
-        for i in range(nb + 3):
-            flush()
-            e0, e1 = qpool[i]
-            e0.record(stream)
+
+        def qpack():
             moe.dispatch_pack_quant(dims, inp.x, b.pos, pq, ps, b.packed_src, stream)
-            e1.record(stream)
-            if i >= 3:
-                qms.append((e0, e1))
-        # and as it is used: route -> count -> quantising pack back to back
-        cms = []
-        cpool = [new_events(2) for _ in range(nb + 3)]
-        host_lead(nb + 3)
-        for i in range(nb + 3):
-            flush()
-            e0, e1 = cpool[i]
-            e0.record(stream)
-            launch("route")
-            launch("count")
-            moe.dispatch_pack_quant(dims, inp.x, b.pos, pq, ps, b.packed_src, stream)
-            e1.record(stream)
-            if i >= 3:
-                cms.append((e0, e1))
-        torch.cuda.synchronize(dev)
-        qm = statistics.mean(a.elapsed_time(c) for a, c in qms)
-        cm = statistics.mean(a.elapsed_time(c) for a, c in cms)
+
+        def chain():
+            run.launch("route")
+            run.launch("count")
+            qpack()
+        qm = run.timed_repeat(qpack, nb, host_lead)
+        cm = run.timed_repeat(chain, nb, host_lead)
         qbytes = w.NT * (2 * w.H + w.R * (w.H + 4 * (w.H // 128))) + w.NT * w.R * 8
         quant = {"ms": qm, "alg_bytes": qbytes, "alg_gbs": qbytes / (qm / 1e3) / 1e9,
                  "frac": qbytes / (qm / 1e3) / 1e9 / measured_peaks()[0],
@@ -534,63 +846,32 @@ def run_ours(args):
                  "note": "moe_dispatch_pack_quant on the same routing, timed alone; "
                          "fp8_dispatch_ms: route + count + quantising pack back to back"}
         del pq, ps
+    out["pack_quant"] = quant
 
     # decode-fused dispatch (route + count + pack in one launch) on the same
     # inputs, when the batch is a decode batch it supports
-    fused = None
-    try:
-        ws = torch.empty(moe.buffer_sizes(dims)["fused_workspace_bytes"], dtype=torch.uint8,
-                         device=dev)
-
-        def fused_call():
-            moe.dispatch_fused(dims, inp.logits, inp.bias, w.score_fn, w.renormalize, inp.x,
-                               inp.x_scales, b.topk_idx, b.topk_w, b.expert_counts,
-                               b.expert_offsets, b.rank_counts, b.rank_offsets, b.send_counts,
-                               b.pos, b.status, b.packed_x, b.packed_scales, b.packed_src, ws,
-                               stream)
-        fe = []
-        fpool = [new_events(2) for _ in range(nb + 3)]
-        host_lead(nb + 3)
-        for i in range(nb + 3):
-            flush()
-            e0, e1 = fpool[i]
-            e0.record(stream)
-            fused_call()
-            e1.record(stream)
-            if i >= 3:
-                fe.append((e0, e1))
-        torch.cuda.synchronize(dev)
-        if moe.read_status(b.status, stream) != moe.MOE_OK:
-            raise RuntimeError("fused dispatch status")
-        fm = statistics.mean(a.elapsed_time(c) for a, c in fe)
-        fused = {"ms": fm, "vs_separate_dispatch_ms": per_timed["dispatch (route+count+pack)"],
-                 "step_ms_if_used": fm + per_timed["combine"],
-                 "note": "moe_dispatch_fused on the same batch (one thread-block cluster for "
-                         "batches of up to 512 tokens, else one cooperative launch)"}
-        del ws
-    except moe.MoeError as ex:
-        fused = {"unsupported": str(ex)}
+    fused = run.fused_ms(nb, host_lead)
+    if "ms" in fused:
+        fused.update({"vs_separate_dispatch_ms": per_timed["dispatch (route+count+pack)"],
+                      "step_ms_if_used": fused["ms"] + per_timed["combine"],
+                      "note": "moe_dispatch_fused on the same batch (one thread-block cluster "
+                              "for batches of up to 512 tokens, else one cooperative launch)"})
+    out["fused_dispatch"] = fused
 
     # the router with the bias in the selection key only (score of the raw
     # logit + bias decides; weights are the raw scores), against the default
     rtimes = {}
     for label, fn in (("default", w.score_fn), ("bias_select_only", w.score_fn | moe.MOE_BIAS_SELECT_ONLY)):
-        rpool = [new_events(2) for _ in range(nb + 3)]
-        host_lead(nb + 3)
-        for i in range(nb + 3):
-            flush()
-            rpool[i][0].record(stream)
-            moe.route_topk(dims, inp.logits, inp.bias, fn, w.renormalize, b.topk_idx, b.topk_w, stream)
-            rpool[i][1].record(stream)
-        torch.cuda.synchronize(dev)
-        rtimes[label] = statistics.mean(a.elapsed_time(c) for a, c in rpool[3:])
+        rtimes[label] = run.timed_repeat(
+            lambda fn=fn: moe.route_topk(dims, inp.logits, inp.bias, fn, w.renormalize, b.topk_idx,
+                                         b.topk_w, stream), nb, host_lead)
     # restore the default routing for the steps below
-    launch("route")
-    launch("count")
+    run.launch("route")
+    run.launch("count")
     torch.cuda.synchronize(dev)
 
     # send-side accumulation (partial rows per token and destination rank,
-    # then their sum) and the expert-parallel local path of one rank
+    # then their sum)
     next_rows = {}
     sz = moe.buffer_sizes(dims)
     P = sz["partial_slots"]
@@ -601,7 +882,7 @@ def run_ours(args):
     ppool = [new_events(3) for _ in range(nb + 3)]
     host_lead(nb + 3)
     for i in range(nb + 3):
-        flush()
+        run.flush()
         e = ppool[i]
         e[0].record(stream)
         moe.combine_partials(dims, b.y, b.pos, b.topk_w, part, slot_rank, stream)
@@ -627,97 +908,13 @@ def run_ours(args):
         "partial_rows_per_token": used / w.NT,
         "note": "moe_combine_partials + moe_combine_reduce_partials; one GPU moves more bytes "
                 "this way than the plain combine (the saving is in data sent between GPUs)"}
-    del part, slot_rank
-    d0 = 0
-    cnt_d = int(b.rank_counts[d0].item())
-    tok_d = int(((b.pos >= d0 * sz["cap_rows"]) & (b.pos < (d0 + 1) * sz["cap_rows"]))
-                .any(dim=1).sum().item())
-    evs3 = []
-    rpool = [(new_events(3), new_events(2)) for _ in range(nb + 3)]
-    host_lead(nb + 3)
-    for i in range(nb + 3):
-        flush()
-        e = rpool[i][0]
-        e[0].record(stream)
-        moe.dispatch_pack_rank(dims, d0, inp.x, inp.x_scales, b.pos, b.packed_x, b.packed_scales,
-                               b.packed_src, stream)
-        e[1].record(stream)
-        flush()
-        e2 = rpool[i][1]
-        e2[0].record(stream)
-        moe.combine_rank(dims, d0, b.y, b.pos, b.topk_w, out2, stream)
-        e2[1].record(stream)
-        if i >= 3:
-            evs3.append((e[0], e[1], e2[0], e2[1]))
-    torch.cuda.synchronize(dev)
-    t_pr = statistics.mean(a.elapsed_time(c) for a, c, _, _ in evs3)
-    t_cr = statistics.mean(a.elapsed_time(c) for _, _, a, c in evs3)
-    rb = W.row_bytes(w)
-    b_pr = tok_d * rb + cnt_d * rb + cnt_d * 8
-    b_cr = cnt_d * yb + w.NT * yb + w.NT * w.R * 8
-    next_rows["ep_local_rank0"] = {
-        "pack_rank_ms": t_pr, "combine_rank_ms": t_cr, "rows": cnt_d, "tokens": tok_d,
-        "pack_rank_alg_gbs": b_pr / (t_pr / 1e3) / 1e9,
-        "combine_rank_alg_gbs": b_cr / (t_cr / 1e3) / 1e9,
-        "note": "moe_dispatch_pack_rank + moe_combine_rank for rank 0 (the all-reduce over "
-                "ranks that completes it is not part of the library)"}
-    del out2
-
-    # ---- end to end through the public API with host buffers -------------
-    e2e = run_e2e(args, w, dims, inp_cpu, b, dev, stream, flush, moe)
-
-    alg = W.algorithmic_bytes(w)
-    peak, peak_kind = measured_peaks()
-    kern = {}
-    for k in KERNELS:
-        mean_ms = statistics.mean(per[k])
-        kern[k] = {"ms": mean_ms, "median_ms": statistics.median(per[k]),
-                   "alg_bytes": alg[k], "alg_gbs": alg[k] / (mean_ms / 1e3) / 1e9}
-    # the dominant kernel by median (a single stalled launch cannot flip it);
-    # its achieved rate below uses the mean launch time
-    dom = max(("pack", "combine"), key=lambda k: kern[k]["median_ms"])
-    # combine has its own events inside the timed region; pack's come from
-    # the breakdown pass right after it
-    dom_ms = per_timed["combine"] if dom == "combine" else kern["pack"]["ms"]
-    achieved = alg[dom] / (dom_ms / 1e3) / 1e9
-    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
-                "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
-                if peak_kind == "measured" else "fallback 6.8 TB/s",
-                "unit": "GB/s", "frac": achieved / peak, "traffic": ncu_traffic(dom, w.name),
-                "alg_bytes_per_launch": alg[dom], "launch_ms": dom_ms}
-    pc_ms = kern["pack"]["ms"] + per_timed["combine"]
-    pc_gbs = (alg["pack"] + alg["combine"]) / (pc_ms / 1e3) / 1e9
-
-    if rank != 0:
-        return 0
-    cpu = None
-    if world == 1 and args.cpu_seconds > 0:
-        import oracle
-        oracle.build_lib()
-        cpu = cpu_baseline(w, inp_cpu, args.cpu_seconds)
-
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "io_dtype": "bf16", "data": "synthetic", "config": workload_config(w),
-        "gpu_launches": 4 * args.steps,
-        "roofline": roofline,
-        "pack_plus_combine": {"ms": pc_ms, "alg_gbs": pc_gbs, "frac": pc_gbs / peak,
-                              "frac_of_8tbs_nominal": pc_gbs / 8000.0},
-        "timed_segments_ms": per_timed,
-        "graph_replay": graph_replay,
-        "pack_quant": quant,
-        "fused_dispatch": fused,
-        "next_rows": next_rows,
-        "kernels": kern,
-        "e2e": e2e,
-        "cpu_baseline": cpu,
-        "clocks": clocks,
-        "wall_s_timed_region": t_wall1 - t_wall0,
-    }
-    print(json.dumps(line))
-    return 0
+    del part, slot_rank, out2
+    ep = run.ep_local(nb, host_lead)
+    ep["note"] = ("moe_dispatch_pack_rank + moe_combine_rank for rank 0 (the all-reduce over "
+                  "ranks that completes it is not part of the library)")
+    next_rows["ep_local_rank0"] = ep
+    out["next_rows"] = next_rows
+    return out
 
 
 def run_e2e(args, w, dims, inp_cpu, b, dev, stream, flush, moe):
