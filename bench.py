@@ -308,6 +308,29 @@ def workload_config(w):
 # GPU arm
 # --------------------------------------------------------------------------
 
+class nvtx_range:
+    """NVTX range around a part of the run (lets a profiler select, e.g., the
+    launches of the timed region); does nothing where NVTX is unavailable."""
+
+    def __init__(self, name):
+        self.name = name
+
+    def __enter__(self):
+        try:
+            import torch
+            torch.cuda.nvtx.range_push(self.name)
+            self.ok = True
+        except Exception:
+            self.ok = False
+        return self
+
+    def __exit__(self, *exc):
+        if self.ok:
+            import torch
+            torch.cuda.nvtx.range_pop()
+        return False
+
+
 def new_events(n):
     import torch
     return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
@@ -647,9 +670,10 @@ def run_ours(args):
         pg.barrier()
     torch.cuda.synchronize(dev)
     t_wall0 = time.time()
-    for e in evs:
-        run.step(e)
-    torch.cuda.synchronize(dev)
+    with nvtx_range("timed"):
+        for e in evs:
+            run.step(e)
+        torch.cuda.synchronize(dev)
     if pg:
         pg.barrier()
     t_wall1 = time.time()
@@ -678,10 +702,15 @@ def run_ours(args):
                  "route+count alone, back to back (diagnostic)": route_count_chain_ms}
     step_wb_ms = reduce_max(statistics.mean(step_ms) + max(0.0, wb["pack"]) + max(0.0, wb["combine"]), pg)
 
+    with nvtx_range("ep_local"):
+        ep_main = run.ep_local(nb, host_lead)
+    ep_main["note"] = ("moe_dispatch_pack_rank + moe_combine_rank for rank 0 (the all-reduce "
+                       "over ranks that completes it is not part of the library)")
     graph_replay = extra = e2e = None
     if not args.no_extras:
         graph_replay = graph_replay_of(args, run, host_lead, pg, world)
         extra = variants_of(args, run, nb, host_lead, per_timed)
+        extra["next_rows"]["ep_local_rank0"] = ep_main
         e2e = run_e2e(args, w, dims, inp_cpu, b, dev, stream, flush, moe)
 
     alg = W.algorithmic_bytes(w)
@@ -763,6 +792,8 @@ def run_ours(args):
     }
     if extra is not None:
         line.update(extra)
+    else:
+        line["next_rows"] = {"ep_local_rank0": ep_main}
     if workloads is not None:
         line["workloads"] = workloads
     print(json.dumps(line))
@@ -909,10 +940,6 @@ def variants_of(args, run, nb, host_lead, per_timed):
         "note": "moe_combine_partials + moe_combine_reduce_partials; one GPU moves more bytes "
                 "this way than the plain combine (the saving is in data sent between GPUs)"}
     del part, slot_rank, out2
-    ep = run.ep_local(nb, host_lead)
-    ep["note"] = ("moe_dispatch_pack_rank + moe_combine_rank for rank 0 (the all-reduce over "
-                  "ranks that completes it is not part of the library)")
-    next_rows["ep_local_rank0"] = ep
     out["next_rows"] = next_rows
     return out
 

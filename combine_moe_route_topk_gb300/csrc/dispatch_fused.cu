@@ -1,62 +1,85 @@
 // Decode-fused dispatch: route top-k, dispatch count and dispatch pack in
-// ONE cooperative launch.
+// one call, as two kernels: route and count in ONE cooperative launch, then
+// the pack kernel of dispatch_pack.cu, launched with programmatic dependent
+// launch so that it is scheduled while the first one runs.
 //
 // "Hosting Qwen on Blackwell", section "Expert parallel": for decode the
 // whole dispatch kernel is fused into one, while prefill splits it into
 // several kernels because routing needs fewer blocks than the rest.
 // "Lower latency and higher throughput with multi-node DeepSeek
 // deployment", section "CUDA Graph": a fixed number of kernels splits the
-// dynamically routed work.  The method of each phase is that of the
-// separate kernels (route_topk.cu, dispatch_count.cu, dispatch_pack.cu) and
-// the outputs are identical to theirs.
+// dynamically routed work.  "Enabling trillion-parameter models on AWS
+// EFA", section "Dispatch and combine": per-expert counts, then their
+// cumulative sum gives the offsets at which tokens are packed per
+// destination.  The outputs are identical to those of the separate kernels
+// (route_topk.cu, dispatch_count.cu, dispatch_pack.cu).
 //
-// Phases, separated by grid-wide barriers (all blocks are co-resident: the
-// kernel is launched cooperatively):
-//   1. route: every warp routes tokens (grid-stride), writing topk_idx/w;
-//   2. count: the first CB = ceil(N*T/256) <= 16 blocks each own 256
-//      consecutive tokens (one per thread), build their histograms in shared
-//      memory as the count kernel does, publish them to the workspace, meet
-//      at a barrier of their own, then each derives offsets, send counts and
-//      the rows of its tokens;
-//   3. pack: every block copies token rows (grid-stride) to their rows.
-// x is an input, not written here: while the count blocks work, the other
-// blocks (idle until the second barrier) ask for the x rows to be brought
-// into L2 (bulk prefetch, evict-last, at most half of the L2), so that
-// pack reads them from L2, and the packed rows are stored with an
-// evict-first hint so that they do not push those rows out.  Measured on
-// the DeepSeek-V3 decode batch (GB300, L2 flushed before each launch):
-// pack phase 65 -> 56 us, count phase 12 -> 18 us (its L2 accesses queue
-// behind the prefetch), whole kernel 118 -> 115 us; issued before routing
-// instead, the prefetches slowed routing from 5.5 to 14 us.  Every barrier
-// wait is bounded: a wait that gives up makes the status word
-// MOE_ERR_TIMEOUT and the kernel returns.
+// The route-count grid is G co-resident blocks (two per SM, launched
+// cooperatively so that all of them are resident at once); block b owns the
+// contiguous tokens [b*NT/G, (b+1)*NT/G), at most 32 of them.
+//   1. route: one warp per token of the block; the selections stay in
+//      shared memory, and a 32-bit mask per expert marks the block's tokens
+//      that chose it (a pair's rank among the block's pairs of its expert is
+//      a population count of the mask below its token);
+//   2. count: the block publishes its per-expert histogram (one byte per
+//      expert) to the workspace and takes a ticket from an arrival counter
+//      (an acquire-release atomic after a block barrier).  The block that
+//      draws the last ticket sums the histograms in chunks of 16 blocks,
+//      scans the chunk sums into per-chunk prefixes and the expert totals
+//      into the offsets, writes the count outputs and releases the others by
+//      bumping a generation word.  The other blocks meanwhile bring their
+//      own x rows into L2 (bulk prefetch, evict-last) and then wait for the
+//      generation word to change (bounded);
+//   3. rows: each block finishes the rows of its own pairs -- expert start
+//      + its chunk's prefix + the histograms of the earlier blocks of its
+//      chunk + the rank inside the block -- and writes pos and its send
+//      counts.
+// Nothing waits for more than one event: no grid-wide barrier, and the
+// histogram exchange is one round trip through L2.  The wait is bounded: a
+// wait that gives up leaves MOE_ERR_TIMEOUT in the status word.  The pack
+// kernel, whose 4096 one-token blocks the hardware spreads over the SMs as
+// they free up, then copies the rows from L2.  A single kernel that also
+// packed (each block its own tokens) took 104 us on the DeepSeek-V3 decode
+// batch: with a fixed share of tokens per block its blocks finished between
+// 58 and 97 us.
 //
-// Scope: decode batches (N*T <= 4096), T % 32 == 0, R <= 8, E <= 512; the
-// host rejects anything else with MOE_ERR_UNSUPPORTED (use the three
-// separate calls).
+// Scope: decode batches (N*T <= 4096), R <= 16, E <= 512; the host rejects
+// anything else with MOE_ERR_UNSUPPORTED (use the three separate calls).
 #include <mutex>
 
 #include <cuda.h>  // CUcontext and CUresult only: the two driver calls are fetched at run time
 
 #include "mem_ops.cuh"
 #include "moe_internal.cuh"
+#include "pdl.cuh"
 #include "route_impl.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kFThreads = 256;  // 8 warps; one token per thread in the count
-constexpr int kFWarps = kFThreads / 32;
-constexpr int kMaxCountBlocks = 16;
-constexpr int kFMaxR = 8;
-constexpr int kSendStage = 2048;               // ints of send staging per count block
-constexpr long long kSpinLimit = 1ll << 20;    // polls per barrier wait (about a second)
+constexpr int kCThreads = 512;                 // 16 warps
+constexpr int kCWarps = kCThreads / 32;
+constexpr int kCMaxTok = 32;                   // tokens per block (32-bit masks)
+constexpr int kCMaxR = 16;                     // pairs per block <= 512 = threads
+constexpr int kCMaxE = 512;
+constexpr int kCMaxGrid = 320;                 // blocks the workspace is sized for
+constexpr int kChunk = 16;                     // blocks per prefix chunk
+constexpr int kMaxChunks = kCMaxGrid / kChunk;
+constexpr int kCMaxNT = 4096;
+constexpr int kSendSmem = 2048;                // ints of send-count staging per block
+constexpr long long kSpinLimit = 1ll << 20;    // polls of the release wait (well under a second)
 
-// workspace words; the grid barrier, the count barrier and the error word
-// sit in different 128-byte lines so that blocks polling one do not slow the
-// atomics of another
-constexpr int kWsGridArrive = 0, kWsGridGen = 1, kWsCntArrive = 32, kWsCntGen = 33, kWsError = 64;
-constexpr int kWsHeader = 96;
+// workspace: words of the arrival counter, generation, error and overflow
+// flag in separate 128-byte lines, then the byte histograms, the chunk
+// prefixes (u16) and the expert offsets
+constexpr int kWsArrive = 0, kWsGen = 32, kWsError = 64, kWsOver = 96;
+constexpr int kWsHeaderBytes = 512;
+
+__host__ __device__ inline int pad16(int v) { return (v + 15) & ~15; }
+__host__ __device__ inline int64_t ws_hist_off() { return kWsHeaderBytes; }
+__host__ __device__ inline int64_t ws_cpre_off(int E) { return ws_hist_off() + (int64_t)kCMaxGrid * pad16(E); }
+__host__ __device__ inline int64_t ws_eoff_off(int E) { return ws_cpre_off(E) + (int64_t)kMaxChunks * pad16(E) * 2; }
+__host__ __device__ inline int64_t ws_bytes(int E) { return ws_eoff_off(E) + pad16((E + 1) * 4); }
 
 struct FusedParams {
     const float *logits;
@@ -65,9 +88,8 @@ struct FusedParams {
     const uint4 *x;
     const float *x_scales;
     int nvec, spr;
-    int N, T, E, R, cap, CB;
+    int N, T, E, R, cap;
     int64_t rows_total;
-    int64_t pf_rows;  // x rows [0, pf_rows) are prefetched into L2 (0: none)
     int32_t *topk_idx;
     float *topk_w;
     int32_t *expert_counts, *expert_offsets, *rank_counts, *rank_offsets, *send_counts, *pos,
@@ -75,8 +97,21 @@ struct FusedParams {
     uint4 *packed_x;
     float *packed_scales;
     int32_t *packed_src;
-    int *ws;
+    unsigned char *ws;
 };
+
+// Ticket of a block: add 1 with acquire-release semantics at GPU scope (the
+// block's earlier writes, ordered before it by a block barrier, are released
+// with it; the holder of the last ticket acquires every other block's).
+__device__ __forceinline__ int atomic_add_acq_rel(int *p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ void red_add_release(int *p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 __device__ __forceinline__ int ld_acquire(const int *p) {
     int v;
@@ -84,402 +119,266 @@ __device__ __forceinline__ int ld_acquire(const int *p) {
     return v;
 }
 
-// Barrier of `nblocks` blocks on (arrive, gen) words of the workspace.
-// Returns false when the wait gave up or another block recorded an error.
 // Polls *word until it differs from `value`, at most `limit` times with a
-// growing sleep between polls (32 ns doubling to 512 ns); false if it gave up.
+// growing sleep between polls (32 ns doubling to 128 ns); false if it gave up.
 __device__ bool wait_while_equal(const int *word, int value, long long limit) {
     long long it = 0;
     unsigned ns = 32;
     while (ld_acquire(word) == value) {
         if (++it > limit) return false;
         __nanosleep(ns);
-        if (ns < 512) ns <<= 1;  // back off: hundreds of blocks poll one word
+        if (ns < 128) ns <<= 1;  // back off: hundreds of blocks poll one word
     }
     return true;
 }
 
-__device__ bool bounded_barrier(int *arrive, int *gen, int nblocks, int *err) {
-    __shared__ int s_ok;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int ok = 1;
-        const int g0 = ld_acquire(gen);
-        __threadfence();  // this block's writes before its arrival
-        if (atomicAdd(arrive, 1) == nblocks - 1) {
-            atomicExch(arrive, 0);
-            __threadfence();
-            atomicAdd(gen, 1);  // release the others
-        } else if (!wait_while_equal(gen, g0, kSpinLimit)) {
-            atomicCAS(err, 0, MOE_ERR_TIMEOUT);
-            ok = 0;
-        }
-        __threadfence();
-        s_ok = ok && ld_acquire(err) == 0;
-    }
-    __syncthreads();
-    return s_ok != 0;
-}
-
-__device__ __forceinline__ unsigned lanemask_lt() {
-    unsigned m;
-    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-    return m;
-}
-
-struct FusedSmem {
-    int gmask, run, base, tot, eoff, fin, send, misc, bytes;
+// Shared-memory layout of the cooperative kernel.  Every section starts on
+// a 16-byte boundary.
+struct CoopSmem {
+    int mask, sel, send, csum, tot, bytes;
 };
 
-// Every section starts on a 16-byte boundary (fin is read as int2).
-__host__ __device__ inline FusedSmem fused_smem_layout(int E) {
-    FusedSmem s;
+__host__ __device__ inline CoopSmem coop_smem_layout(int E) {
+    CoopSmem s;
     int o = 0;
     auto take = [&o](int bytes) {
         const int at = o;
-        o += (bytes + 15) & ~15;
+        o += pad16(bytes);
         return at;
     };
-    s.gmask = take(kFWarps * E * 4);  // group masks, then group prefixes
-    s.run = take(E * 4);              // this block's histogram
-    s.base = take(E * 4);             // pairs in earlier count blocks
-    s.tot = take(E * 4);              // pairs in all count blocks
-    s.eoff = take((E + 1) * 4);       // exclusive scan of tot
-    s.fin = take(E * 8);              // first row / rows left per expert
-    s.send = take(kSendStage * 4);    // send counts of this block's source ranks
-    s.misc = take(64 * 4);            // flags and scan partials
+    s.mask = take(E * 4);                        // u32 per expert: tokens of the block that chose it
+    s.sel = take(kCMaxTok * kCMaxR * 4);         // selected experts of the block's pairs
+    s.send = take(kSendSmem * 4);                // send counts of the block's source ranks
+    s.csum = take(kMaxChunks * pad16(E) * 2);    // last block: chunk sums (u16)
+    s.tot = take((E + 1) * 4);                   // last block: totals, then offsets
     s.bytes = o;
     return s;
 }
 
-constexpr int kPackU = 4;  // 16-byte vectors of a row per thread in flight (pack)
-
-// 3 co-resident blocks per SM.  4 (64 registers per thread, no spills for
-// up to 8 experts per lane) routes a 4096-token batch in one pass, but the
-// whole kernel took longer on the DeepSeek-V3 decode batch (123 vs 115 us).
 template <int J, bool kVec4>
-__global__ void __launch_bounds__(kFThreads, 3)
-dispatch_fused_kernel(FusedParams P) {
+__global__ void __launch_bounds__(kCThreads, 2)
+route_count_kernel(FusedParams P) {
     extern __shared__ __align__(16) unsigned char smem[];
-    __shared__ int s_pos[kFMaxR];
+    __shared__ int s_flag[4];  // [0] last ticket, [1] released, [2] generation seen at start
+    __shared__ int s_wsum[kCWarps];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int NT = P.N * P.T;
-    int *err = P.ws + kWsError;
+    const int NT = P.N * P.T, E = P.E, R = P.R, N = P.N, T = P.T, L = E / N;
+    const int G = (int)gridDim.x, b = (int)blockIdx.x;
+    const int Ep = pad16(E);
+    const CoopSmem lay = coop_smem_layout(E);
+    uint32_t *mask = reinterpret_cast<uint32_t *>(smem + lay.mask);
+    int *sel = reinterpret_cast<int *>(smem + lay.sel);
+    int *ssend = reinterpret_cast<int *>(smem + lay.send);
+    int *ws_words = reinterpret_cast<int *>(P.ws);
+    unsigned char *ws_hist = P.ws + ws_hist_off();
+    uint16_t *ws_cpre = reinterpret_cast<uint16_t *>(P.ws + ws_cpre_off(E));
+    int *ws_eoff = reinterpret_cast<int *>(P.ws + ws_eoff_off(E));
 
-    // ---- phase 1: route ------------------------------------------------------
-    for (int64_t g = (int64_t)blockIdx.x * kFWarps + warp; g < NT; g += (int64_t)gridDim.x * kFWarps)
-        route_impl::route_token<J, kVec4>(P.logits, P.bias, g, P.E, P.R, P.score_fn,
-                                          P.renormalize, P.topk_idx, P.topk_w, lane);
-    bool alive = bounded_barrier(P.ws + kWsGridArrive, P.ws + kWsGridGen, gridDim.x, err);
+    const int tb = (int)((int64_t)b * NT / G), te = (int)((int64_t)(b + 1) * NT / G);
+    const int ntok = te - tb;  // <= 32, checked by the launcher
+    const int npair = ntok * R;
+    const int s_first = tb / T;
+    const int span = ntok > 0 ? (te - 1) / T - s_first + 1 : 0;
+    const bool smem_send = span * N <= kSendSmem;
 
-    // ---- phase 2: count (blocks 0 .. CB-1) -------------------------------------
-    const int b = blockIdx.x;
-    // meanwhile the other blocks prefetch x, one row per lane of warp 0
-    const int nb = (int)gridDim.x - P.CB;
-    if (alive && b >= P.CB && warp == 0) {
+    // the pack kernel that follows may be scheduled now: it reads nothing of
+    // this kernel's before its own grid-dependency wait
+    grid_launch_dependents();
+    if (tid == 0) s_flag[2] = ld_acquire(ws_words + kWsGen);  // before this block's ticket
+    for (int i = tid; i < E; i += kCThreads) mask[i] = 0u;
+    if (smem_send)
+        for (int i = tid; i < span * N; i += kCThreads) ssend[i] = 0;
+    __syncthreads();
+
+    // ---- 1. route ---------------------------------------------------------------
+    for (int t = warp; t < ntok; t += kCWarps) {
+        const int e = route_impl::route_token<J, kVec4>(P.logits, P.bias, (int64_t)(tb + t), E, R, P.score_fn,
+                                                        P.renormalize, P.topk_idx, P.topk_w, lane);
+        if (lane < R) sel[t * R + lane] = e;
+    }
+    __syncthreads();
+    if (tid < npair) atomicOr(mask + sel[tid], 1u << (tid / R));
+    __syncthreads();
+
+    // ---- 2. count: publish, ticket, the last block scans --------------------------
+    for (int e = tid; e < Ep; e += kCThreads)
+        ws_hist[(int64_t)b * Ep + e] = (unsigned char)(e < E ? __popc(mask[e]) : 0);
+    __syncthreads();  // the block's histogram bytes, released by its ticket
+    if (tid == 0) s_flag[0] = atomic_add_acq_rel(ws_words + kWsArrive, 1) == G - 1;
+    __syncthreads();
+    if (s_flag[0]) {
+        // the last ticket acquired every other block's histogram
+        uint16_t *csum = reinterpret_cast<uint16_t *>(smem + lay.csum);
+        int *tot = reinterpret_cast<int *>(smem + lay.tot);
+        const int C = (G + kChunk - 1) / kChunk;
+        const int nv = Ep / 16;  // 16-byte vectors of a histogram row
+        // chunk sums: item (chunk c, vector v) adds 16 blocks' 16 bytes
+        for (int it = tid; it < C * nv; it += kCThreads) {
+            const int c = it / nv, v = it - c * nv;
+            uint4 h[kChunk];
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j) {
+                const int bb = c * kChunk + j;
+                h[j] = bb < G ? __ldcg(reinterpret_cast<const uint4 *>(ws_hist + (int64_t)bb * Ep) + v)
+                              : make_uint4(0u, 0u, 0u, 0u);
+            }
+            // bytes 0,2 / 1,3 of every word summed in 16-bit halves (a chunk
+            // sum is at most 16 * 32 = 512)
+            uint32_t ev[4] = {0u, 0u, 0u, 0u}, od[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j) {
+                const uint32_t w4[4] = {h[j].x, h[j].y, h[j].z, h[j].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    ev[q] += w4[q] & 0x00ff00ffu;
+                    od[q] += (w4[q] >> 8) & 0x00ff00ffu;
+                }
+            }
+            uint16_t *dst = csum + c * Ep + v * 16;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                dst[4 * q + 0] = (uint16_t)(ev[q] & 0xffffu);
+                dst[4 * q + 1] = (uint16_t)(od[q] & 0xffffu);
+                dst[4 * q + 2] = (uint16_t)(ev[q] >> 16);
+                dst[4 * q + 3] = (uint16_t)(od[q] >> 16);
+            }
+        }
+        __syncthreads();
+        // per expert: exclusive prefix over chunks (to the workspace) and total
+        for (int e = tid; e < Ep; e += kCThreads) {
+            int run = 0;
+            for (int c = 0; c < C; ++c) {
+                ws_cpre[c * Ep + e] = (uint16_t)run;
+                run += csum[c * Ep + e];
+            }
+            if (e < E) tot[e] = run;
+        }
+        __syncthreads();
+        // exclusive scan of the totals over experts (E <= 512: one per thread)
+        const int v0 = tid < E ? tot[tid] : 0;
+        int xs = v0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, xs, off);
+            if (lane >= off) xs += y;
+        }
+        if (lane == 31) s_wsum[warp] = xs;
+        __syncthreads();
+        if (warp == 0) {
+            int sv = lane < kCWarps ? s_wsum[lane] : 0;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, sv, off);
+                if (lane >= off) sv += y;
+            }
+            if (lane < kCWarps) s_wsum[lane] = sv;  // inclusive over warps
+        }
+        __syncthreads();
+        const int excl = xs - v0 + (warp > 0 ? s_wsum[warp - 1] : 0);
+        __syncthreads();  // every total read before it is overwritten
+        if (tid < E) {
+            tot[tid] = excl;
+            P.expert_counts[tid] = v0;
+            P.expert_offsets[tid] = excl;
+            ws_eoff[tid] = excl;
+            if (tid == E - 1) {
+                tot[E] = excl + v0;
+                P.expert_offsets[E] = excl + v0;
+                ws_eoff[E] = excl + v0;
+            }
+        }
+        __syncthreads();
+        int over = 0;
+        for (int d = tid; d < N; d += kCThreads) {
+            const int rc = tot[(d + 1) * L] - tot[d * L];
+            P.rank_counts[d] = rc;
+            P.rank_offsets[d] = tot[d * L];
+            over |= rc > P.cap;
+        }
+        over = __syncthreads_or(over);
+        for (int i = tid; i < N * N; i += kCThreads) P.send_counts[i] = 0;  // filled after the release
+        if (tid == 0) {
+            P.rank_offsets[N] = tot[E];
+            *P.status = over ? MOE_ERR_CAPACITY : MOE_OK;
+            ws_words[kWsOver] = over;
+        }
+        __syncthreads();  // every thread's prefixes, offsets and zeroed send counts
+        if (tid == 0) {
+            atomicExch(ws_words + kWsArrive, 0);  // ready for the next launch
+            red_add_release(ws_words + kWsGen, 1);  // release the others
+            s_flag[1] = 1;
+        }
+    } else {
+        // while the last block scans: this block's x rows into L2, then the wait
+        if (warp == 0) {
+            const uint64_t keep = l2_policy_evict_last();
+            const uint32_t rb = (uint32_t)P.nvec * 16u;
+            if (rb <= 65536u)
+                for (int t = lane; t < ntok; t += 32) prefetch_l2(P.x + (int64_t)(tb + t) * P.nvec, rb, keep);
+        }
+        if (tid == 0) {
+            const bool ok = wait_while_equal(ws_words + kWsGen, s_flag[2], kSpinLimit);
+            if (!ok) atomicCAS(ws_words + kWsError, 0, MOE_ERR_TIMEOUT);
+            s_flag[1] = ok;
+        }
+    }
+    __syncthreads();
+    if (!s_flag[1]) {
+        if (tid == 0) *P.status = MOE_ERR_TIMEOUT;
+        return;
+    }
+
+    // ---- 3. rows of this block's pairs, send counts -----------------------------
+    if (tid < npair) {
+        const int t = tid / R, k = tid - t * R;
+        const int g = tb + t;
+        const int e = sel[tid], d = e / L;
+        const int c = b / kChunk;
+        int base = __ldcg(ws_cpre + c * Ep + e);  // written by the last block before the release
+        for (int bb = c * kChunk; bb < b; ++bb) base += __ldcg(ws_hist + (int64_t)bb * Ep + e);
+        const int in_block = __popc(mask[e] & ((1u << t) - 1u));
+        const int local = __ldcg(ws_eoff + e) - __ldcg(ws_eoff + d * L) + base + in_block;
+        const int p = local < P.cap ? d * P.cap + local : -1;
+        P.pos[(int64_t)g * R + k] = p;
+        // counts report demand: the pair is counted whether or not it fits
+        if (smem_send) atomicAdd(ssend + (g / T - s_first) * N + d, 1);
+        else atomicAdd(P.send_counts + (int64_t)(g / T) * N + d, 1);
+    }
+    __syncthreads();
+    if (smem_send)
+        for (int i = tid; i < span * N; i += kCThreads)
+            if (ssend[i]) atomicAdd(P.send_counts + (int64_t)(s_first + i / N) * N + (i - (i / N) * N), ssend[i]);
+
+    // the last block's own rows (the others fetched theirs while waiting)
+    if (s_flag[0] && warp == 0) {
         const uint64_t keep = l2_policy_evict_last();
-        for (int64_t r = (b - P.CB) + (int64_t)lane * nb; r < P.pf_rows; r += 32ll * nb)
-            prefetch_l2(P.x + r * P.nvec, (uint32_t)P.nvec * 16u, keep);
+        const uint32_t rb = (uint32_t)P.nvec * 16u;
+        if (rb <= 65536u)
+            for (int t = lane; t < ntok; t += 32) prefetch_l2(P.x + (int64_t)(tb + t) * P.nvec, rb, keep);
     }
-    if (alive && b < P.CB) {
-        const int E = P.E, N = P.N, T = P.T, R = P.R, L = E / N, CB = P.CB;
-        const FusedSmem lay = fused_smem_layout(E);
-        uint32_t *gmask = reinterpret_cast<uint32_t *>(smem + lay.gmask);
-        int *run = reinterpret_cast<int *>(smem + lay.run);
-        int *sbase = reinterpret_cast<int *>(smem + lay.base);
-        int *stot = reinterpret_cast<int *>(smem + lay.tot);
-        int *eoff = reinterpret_cast<int *>(smem + lay.eoff);
-        int2 *fin = reinterpret_cast<int2 *>(smem + lay.fin);
-        int *ssend = reinterpret_cast<int *>(smem + lay.send);
-        int *misc = reinterpret_cast<int *>(smem + lay.misc);  // [0] bad, [1] over, [16..48) scan
-        int *ws_hist = P.ws + kWsHeader;                            // [CB][E]
-        int *ws_send = ws_hist + kMaxCountBlocks * E;               // [CB][kSendStage]
-        int *ws_bad = ws_send + kMaxCountBlocks * kSendStage;       // [CB]
-
-        const int lo = b * kFThreads, hi = min(NT, lo + kFThreads);
-        const int s_first = lo / T;
-        const int span = (hi - 1) / T - s_first + 1;
-        for (int i = tid; i < kFWarps * E; i += kFThreads) gmask[i] = 0u;
-        for (int i = tid; i < E; i += kFThreads) run[i] = 0;
-        for (int i = tid; i < span * N; i += kFThreads) ssend[i] = 0;
-        if (tid == 0) misc[0] = 0;
-        __syncthreads();
-
-        const int g = lo + tid;
-        const bool active = g < hi;
-        int ek[kFMaxR], part[kFMaxR];
-#pragma unroll
-        for (int k = 0; k < kFMaxR; ++k) {
-            ek[k] = -1;
-            part[k] = 0;
-            if (k < R && active) ek[k] = __ldcg(P.topk_idx + (int64_t)g * R + k);  // written in phase 1
-        }
-        bool bad = false;
-#pragma unroll
-        for (int k = 0; k < kFMaxR; ++k) {
-            if (k < R && active) {
-                const int e = ek[k];
-                bool ok = (e >= 0 && e < E);
-#pragma unroll
-                for (int k2 = 0; k2 < k; ++k2) ok = ok && (ek[k2] != e);
-                if (!ok) {
-                    ek[k] = -1;
-                    bad = true;
-                }
-            }
-        }
-        uint32_t *mymask = gmask + warp * E;
-#pragma unroll
-        for (int k = 0; k < kFMaxR; ++k)
-            if (k < R && ek[k] >= 0) atomicOr(mymask + ek[k], 1u << lane);
-        __syncwarp();
-        const unsigned lt = lanemask_lt();
-#pragma unroll
-        for (int k = 0; k < kFMaxR; ++k)
-            if (k < R && ek[k] >= 0) part[k] = __popc(mymask[ek[k]] & lt);
-        if (bad) atomicOr(misc, 1);
-        __syncthreads();
-        // group prefixes, histogram and send counts (groups never straddle
-        // source ranks: T % 32 == 0)
-        for (int e = tid; e < E; e += kFThreads) {
-            int c[kFWarps];
-#pragma unroll
-            for (int w = 0; w < kFWarps; ++w) c[w] = __popc(gmask[w * E + e]);
-            int r = 0, acc = 0, s_cur = s_first;
-            const int d = e / L;
-#pragma unroll
-            for (int w = 0; w < kFWarps; ++w) {
-                gmask[w * E + e] = (uint32_t)r;
-                r += c[w];
-                const int gw = lo + 32 * w;
-                if (gw < hi) {
-                    if (gw / T != s_cur) {
-                        if (acc) atomicAdd(ssend + (s_cur - s_first) * N + d, acc);
-                        acc = 0;
-                        s_cur = gw / T;
-                    }
-                    acc += c[w];
-                }
-            }
-            if (acc) atomicAdd(ssend + (s_cur - s_first) * N + d, acc);
-            run[e] = r;
-        }
-        __syncthreads();
-        int any_bad = 0;
-        if (CB == 1) {
-            // a single count block: its own histogram and send counts are final
-            for (int e = tid; e < E; e += kFThreads) {
-                sbase[e] = 0;
-                stot[e] = run[e];
-            }
-            for (int i = tid; i < N * N; i += kFThreads) {
-                const int s = i / N, d = i - (i / N) * N;
-                P.send_counts[i] = (s >= s_first && s < s_first + span) ? ssend[(s - s_first) * N + d] : 0;
-            }
-            any_bad = __syncthreads_or(misc[0]);
-        } else {
-            // publish this block's histogram, send counts and flag
-            for (int e = tid; e < E; e += kFThreads) ws_hist[b * E + e] = run[e];
-            for (int i = tid; i < span * N; i += kFThreads) ws_send[b * kSendStage + i] = ssend[i];
-            if (tid == 0) ws_bad[b] = misc[0];
-            alive = bounded_barrier(P.ws + kWsCntArrive, P.ws + kWsCntGen, CB, err);
-            if (alive) {
-                // every workspace load of an item is issued before any is used
-                for (int e = tid; e < E; e += kFThreads) {
-                    int v[kMaxCountBlocks];
-#pragma unroll
-                    for (int bb = 0; bb < kMaxCountBlocks; ++bb)
-                        v[bb] = (bb < CB) ? __ldcg(ws_hist + bb * E + e) : 0;
-                    int base = 0, tot = 0;
-#pragma unroll
-                    for (int bb = 0; bb < kMaxCountBlocks; ++bb) {
-                        tot += v[bb];
-                        if (bb < b) base += v[bb];
-                    }
-                    sbase[e] = base;
-                    stot[e] = tot;
-                }
-                // send_counts rows, split over the count blocks
-                for (int i = b * kFThreads + tid; i < N * N; i += CB * kFThreads) {
-                    const int s = i / N, d = i - (i / N) * N;
-                    const int b_lo = (s * T) / kFThreads;
-                    const int b_hi = min(CB - 1, ((s + 1) * T - 1) / kFThreads);
-                    int v[kMaxCountBlocks];
-#pragma unroll
-                    for (int j = 0; j < kMaxCountBlocks; ++j) {
-                        const int bb = b_lo + j;
-                        v[j] = (bb <= b_hi)
-                                   ? __ldcg(ws_send + bb * kSendStage + (s - (bb * kFThreads) / T) * N + d)
-                                   : 0;
-                    }
-                    int sum = 0;
-#pragma unroll
-                    for (int j = 0; j < kMaxCountBlocks; ++j) sum += v[j];
-                    P.send_counts[i] = sum;
-                }
-                for (int bb = tid; bb < CB; bb += kFThreads) any_bad |= __ldcg(ws_bad + bb);
-            }
-            any_bad = __syncthreads_or(any_bad);
-        }
-        if (alive) {
-            // exclusive scan of stot over experts (E <= 512: 2 per thread)
-            {
-                const int ipt = (E + kFThreads - 1) / kFThreads;
-                int v0 = 0, v1 = 0;
-                if (tid * ipt < E) v0 = stot[tid * ipt];
-                if (ipt > 1 && tid * ipt + 1 < E) v1 = stot[tid * ipt + 1];
-                const int local = v0 + v1;
-                int x = local;
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const int y = __shfl_up_sync(0xffffffffu, x, off);
-                    if (lane >= off) x += y;
-                }
-                int *wsum = misc + 16;
-                if (lane == 31) wsum[warp] = x;
-                __syncthreads();
-                if (warp == 0) {
-                    int sv = (lane < kFWarps) ? wsum[lane] : 0;
-#pragma unroll
-                    for (int off = 1; off < 32; off <<= 1) {
-                        const int y = __shfl_up_sync(0xffffffffu, sv, off);
-                        if (lane >= off) sv += y;
-                    }
-                    if (lane < kFWarps) wsum[lane] = sv;
-                }
-                __syncthreads();
-                int start = x - local + (warp > 0 ? wsum[warp - 1] : 0);
-                if (tid * ipt < E) {
-                    eoff[tid * ipt] = start;
-                    start += v0;
-                    if (tid * ipt == E - 1) eoff[E] = start;
-                }
-                if (ipt > 1 && tid * ipt + 1 < E) {
-                    eoff[tid * ipt + 1] = start;
-                    start += v1;
-                    if (tid * ipt + 1 == E - 1) eoff[E] = start;
-                }
-                __syncthreads();
-            }
-            int over = 0;
-            for (int d = tid; d < N; d += kFThreads)
-                if (eoff[(d + 1) * L] - eoff[d * L] > P.cap) over = 1;
-            over = __syncthreads_or(over);
-            for (int e = tid; e < E; e += kFThreads) {
-                const int d = e / L;
-                const int local = eoff[e] - eoff[d * L] + sbase[e];
-                fin[e] = make_int2(d * P.cap + local, P.cap - local);
-                if (!over) {
-#pragma unroll
-                    for (int w = 0; w < kFWarps; ++w) gmask[w * E + e] += (uint32_t)(d * P.cap + local);
-                }
-            }
-            __syncthreads();
-            if (b == 0) {
-                for (int e = tid; e < E; e += kFThreads) {
-                    P.expert_counts[e] = stot[e];
-                    P.expert_offsets[e] = eoff[e];
-                }
-                for (int d = tid; d < N; d += kFThreads) {
-                    P.rank_counts[d] = eoff[(d + 1) * L] - eoff[d * L];
-                    P.rank_offsets[d] = eoff[d * L];
-                }
-                if (tid == 0) {
-                    P.expert_offsets[E] = eoff[E];
-                    P.rank_offsets[N] = eoff[E];
-                    *P.status = any_bad ? MOE_ERR_INVALID_ARG : (over ? MOE_ERR_CAPACITY : MOE_OK);
-                }
-            }
-            if (active) {
-#pragma unroll
-                for (int k = 0; k < kFMaxR; ++k) {
-                    if (k < R) {
-                        int out = -1;
-                        if (ek[k] >= 0) {
-                            const int pr = (int)mymask[ek[k]] + part[k];
-                            if (!over) out = pr;
-                            else {
-                                const int2 f = fin[ek[k]];
-                                const int rel = pr;  // prefix without the expert start
-                                out = (rel < f.y) ? f.x + rel : -1;
-                            }
-                        }
-                        P.pos[(int64_t)g * R + k] = out;
-                    }
-                }
-            }
-        }
-    }
-    alive = bounded_barrier(P.ws + kWsGridArrive, P.ws + kWsGridGen, gridDim.x, err) && alive;
-
-    // ---- phase 3: pack --------------------------------------------------------
-    if (alive) {
-        const uint64_t stream_out = l2_policy_evict_first();
-        for (int64_t g = blockIdx.x; g < NT; g += gridDim.x) {
-            if (tid < P.R) {
-                const int p = __ldcg(P.pos + g * P.R + tid);  // written in phase 2
-                const bool ok = p >= 0 && (int64_t)p < P.rows_total;
-                s_pos[tid] = ok ? p : -1;
-                if (ok) P.packed_src[p] = (int32_t)(g * P.R + tid);
-            }
-            __syncthreads();
-            for (int c0 = tid; c0 < P.nvec; c0 += kFThreads * kPackU) {
-                uint4 v[kPackU];
-#pragma unroll
-                for (int u = 0; u < kPackU; ++u) {
-                    const int c = c0 + u * kFThreads;
-                    if (c < P.nvec) v[u] = ld_stream(P.x + g * P.nvec + c);
-                }
-                for (int k = 0; k < P.R; ++k) {
-                    const int p = s_pos[k];
-                    if (p < 0) continue;
-                    uint4 *dst = P.packed_x + (int64_t)p * P.nvec;
-#pragma unroll
-                    for (int u = 0; u < kPackU; ++u) {
-                        const int c = c0 + u * kFThreads;
-                        if (c < P.nvec) st_evict_first(dst + c, v[u], stream_out);
-                    }
-                }
-            }
-            if (P.spr > 0) {
-                for (int i = tid; i < P.R * P.spr; i += kFThreads) {
-                    const int k = i / P.spr, j = i - k * P.spr;
-                    const int p = s_pos[k];
-                    if (p >= 0) P.packed_scales[(int64_t)p * P.spr + j] = __ldg(P.x_scales + g * P.spr + j);
-                }
-            }
-            __syncthreads();
-        }
-    }
-    if (!alive && blockIdx.x == 0 && tid == 0) *P.status = MOE_ERR_TIMEOUT;
 }
 
 template <int J, bool kVec4>
 cudaError_t launch_fused_jv(FusedParams P, cudaStream_t stream) {
-    auto kern = dispatch_fused_kernel<J, kVec4>;
-    const size_t smem = (size_t)fused_smem_layout(P.E).bytes;
+    auto kern = route_count_kernel<J, kVec4>;
+    const size_t smem = (size_t)coop_smem_layout(P.E).bytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCThreads, smem);
     if (e != cudaSuccess) return e;
     const int sms = sm_count();
     if (per_sm < 1 || sms < 1) return cudaErrorNotSupported;
-    int grid = sms * per_sm;
     const int NT = P.N * P.T;
-    const int need = (NT + kFWarps - 1) / kFWarps;  // one routing warp per token is plenty
-    if (grid > need) grid = need;
-    if (grid < P.CB) return cudaErrorNotSupported;
-    // L2 prefetch of x: rows of at most 64 KB filling at most half the L2
-    const int64_t row_bytes = (int64_t)P.nvec * 16;
-    P.pf_rows = row_bytes <= 65536 ? (l2_bytes() / 2) / row_bytes : 0;
-    if (P.pf_rows > NT) P.pf_rows = NT;
-    if (P.pf_rows < 0) P.pf_rows = 0;
-    e = cudaMemsetAsync(P.ws, 0, kWsHeader * sizeof(int), stream);  // barrier words
+    int grid = sms * per_sm;
+    if (grid > kCMaxGrid) grid = kCMaxGrid;
+    if (grid > NT) grid = NT;
+    if ((NT + grid - 1) / grid > kCMaxTok) return cudaErrorNotSupported;  // too few co-resident blocks
+    e = cudaMemsetAsync(P.ws, 0, kWsHeaderBytes, stream);  // arrival counter, generation, flags
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kFThreads);
+    cfg.blockDim = dim3(kCThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -501,21 +400,17 @@ cudaError_t launch_fused_j(FusedParams P, cudaStream_t stream) {
 
 }  // namespace
 
-int64_t fused_workspace_bytes(int E) {
-    return (int64_t)(kWsHeader + kMaxCountBlocks * E + kMaxCountBlocks * kSendStage + kMaxCountBlocks) *
-           (int64_t)sizeof(int);
-}
+int64_t fused_workspace_bytes(int E) { return ws_bytes(E); }
 
 // Empty string when the fused kernel handles these dimensions, else why not.
 namespace {
 // Limits of the cooperative kernel ("" when it can run the batch).
 const char *cooperative_unsupported(int N, int T, int E, int R) {
     const int64_t NT = (int64_t)N * T;
-    if (R > kFMaxR) return "R > 8";
-    if (E > 512) return "E > 512";
-    if (T % 32 != 0) return "T is not a multiple of 32";
-    if (NT > (int64_t)kMaxCountBlocks * kFThreads) return "N*T > 4096 (not a decode batch)";
-    if (NT > 0 && (int64_t)(kFThreads / T + 2) * N > kSendStage) return "too many ranks per count block";
+    if (R > kCMaxR) return "R > 16";
+    if (E > kCMaxE) return "E > 512";
+    if (NT > kCMaxNT) return "N*T > 4096 (not a decode batch)";
+    (void)T;
     return "";
 }
 }  // namespace
@@ -540,7 +435,7 @@ cudaError_t launch_dispatch_fused(const float *logits, const float *bias, int sc
     if ((int64_t)N * T == 0)
         return launch_dispatch_count(topk_idx, N, T, E, R, cap, expert_counts, expert_offsets, rank_counts,
                                      rank_offsets, send_counts, pos, status, stream);
-    // Small batches: one thread-block cluster, no grid barriers and no
+    // Small batches: one thread-block cluster, no grid-wide wait and no
     // workspace (the cooperative kernel below handles everything else, and
     // takes over if the device cannot schedule the cluster).
     if (dispatch_small_eligible((int64_t)N * T, E, R, row_bytes)) {
@@ -567,8 +462,6 @@ cudaError_t launch_dispatch_fused(const float *logits, const float *bias, int sc
     P.E = E;
     P.R = R;
     P.cap = (int)cap;
-    P.CB = (int)(((int64_t)N * T + kFThreads - 1) / kFThreads);
-    if (P.CB < 1) P.CB = 1;
     P.rows_total = (int64_t)N * cap;
     P.topk_idx = topk_idx;
     P.topk_w = topk_w;
@@ -582,24 +475,32 @@ cudaError_t launch_dispatch_fused(const float *logits, const float *bias, int sc
     P.packed_x = reinterpret_cast<uint4 *>(packed_x);
     P.packed_scales = packed_scales;
     P.packed_src = packed_src;
-    P.ws = reinterpret_cast<int *>(workspace);
+    P.ws = reinterpret_cast<unsigned char *>(workspace);
     const int need = (E + 31) / 32;
     // the same experts per lane as the route kernel, so that the softmax
     // denominator is summed in the same order and the weights agree bit for bit
-    if (need <= 1) return launch_fused_j<1>(P, stream);
-    if (need <= 2) return launch_fused_j<2>(P, stream);
-    if (need <= 4) return launch_fused_j<4>(P, stream);
-    if (need <= 8) return launch_fused_j<8>(P, stream);
-    if (need <= 12) return launch_fused_j<12>(P, stream);
-    return launch_fused_j<16>(P, stream);
+    cudaError_t e;
+    if (need <= 1) e = launch_fused_j<1>(P, stream);
+    else if (need <= 2) e = launch_fused_j<2>(P, stream);
+    else if (need <= 4) e = launch_fused_j<4>(P, stream);
+    else if (need <= 8) e = launch_fused_j<8>(P, stream);
+    else if (need <= 12) e = launch_fused_j<12>(P, stream);
+    else e = launch_fused_j<16>(P, stream);
+    if (e != cudaSuccess) return e;
+    // pack: scheduled while the cooperative kernel runs, it waits for it
+    // (rows from pos) and then copies from L2 the x rows that the route-count
+    // blocks prefetched while they waited
+    return launch_dispatch_pack(x, x_scales, pos, (int64_t)N * T, R, row_bytes, spr, (int64_t)N * cap,
+                                packed_x, packed_scales, packed_src, stream);
 }
 
 }  // namespace moe
 
 // ---- self-test of the bounded wait -----------------------------------------
 //
-// One thread waits, through the same bounded poll as the grid barriers, for
-// status[1] to become nonzero; status[0] gets MOE_OK if it did and
+// One thread waits, through the same bounded poll as the route-count
+// kernel's release wait, for status[1] to become nonzero; status[0] gets
+// MOE_OK if it did and
 // MOE_ERR_TIMEOUT if the wait gave up.  Nothing in the library writes
 // status[1], so unless the caller set it beforehand the wait runs out: this
 // shows on a given GPU that a wait which is never satisfied ends with a

@@ -213,13 +213,19 @@ int moe_dispatch_pack(const MoeDims *dims, const void *x, const float *x_scales,
  *     cluster whose blocks own 32 tokens each and exchange only per-expert
  *     counts through distributed shared memory (no grid barrier; the
  *     workspace is not touched);
- *   - otherwise N*T <= 4096, T % 32 == 0, R <= 8, E <= 512: a cooperative
- *     launch (all its blocks are resident at once) whose phases meet at
- *     grid-wide barriers; each barrier wait is bounded, and one that gives
- *     up leaves MOE_ERR_TIMEOUT in *status.  On GB300 the fused call beats the three
- * separate calls only for small rows (up to about 200 KB of row traffic
- * per 32 tokens, e.g. 256 tokens with R = 2 and 2 KB rows: 12.4 vs 15.4 us);
- * beyond that the separate calls, whose pack uses every SM, are faster.
+ *   - otherwise N*T <= 4096, R <= 16, E <= 512, any T: route and count in
+ *     one cooperative launch (all its blocks resident at once, two per SM,
+ *     each routing and counting its own run of at most 32 tokens; the
+ *     per-block histograms meet in the workspace, where the block that
+ *     finishes last scans them and releases the others), then the pack
+ *     kernel, which starts as the first one ends.  The wait for the release
+ *     is bounded; one that gives up leaves MOE_ERR_TIMEOUT in *status.  The
+ *     call clears the workspace's first 512 bytes before the launch.
+ * On GB300 the fused call beats the three separate calls only on small
+ * batches with small rows (256 tokens with R = 2 and 2 KB rows: 12.8 vs
+ * 15.7 us).  On the 4096-token DeepSeek-V3- and Kimi-K2-shaped decode
+ * batches the separate calls, which already overlap their launches, are
+ * faster (DeepSeek-V3: about 95 vs 87 us). 
  * An empty batch (N*T == 0) is always accepted: like moe_dispatch_count it
  * writes zero counts and offsets and MOE_OK (the workspace is not touched). */
 int moe_dispatch_fused(const MoeDims *dims, const float *logits, const float *bias, int score_fn,
@@ -239,7 +245,7 @@ int moe_dispatch_fused(const MoeDims *dims, const float *logits, const float *bi
  *   Scratch: a fixed array of 192 KiB in the library's device memory,
  *   reserved on every GPU that loads the library until the process exits
  *   (enough for every batch moe_dispatch_fused accepts: E <= 512 needs at
- *   most 164,288 bytes; larger needs are rejected with MOE_ERR_UNSUPPORTED).
+ *   most 186,896 bytes; larger needs are rejected with MOE_ERR_UNSUPPORTED).
  *   The first call on a device looks up the array's device address (with
  *   that device current); make that first call before any stream capture.
  *   The address is cached per device and CUDA context: after
@@ -337,10 +343,10 @@ int moe_read_status(const int32_t *status, void *stream);
 
 /* Self-test of the library's bounded waits (the pages have no counterpart:
  * this is a diagnostic of this implementation).  Enqueues one thread that
- * waits, with the same bounded poll the decode-fused kernel uses at its
- * grid barriers (a sleep of 32 ns doubling to 512 ns between polls), for
+ * waits, with the same bounded poll the decode-fused kernel uses for its
+ * release (a sleep of 32 ns doubling to 128 ns between polls), for
  * status[1] to become nonzero, at most `polls` times (1 <= polls <= 2^20,
- * about half a second at the upper end).  status[0] then becomes MOE_OK if
+ * well under a second at the upper end).  status[0] then becomes MOE_OK if
  * the word changed and MOE_ERR_TIMEOUT if the wait gave up.  Nothing in the
  * library writes status[1]: left at zero, the wait runs out, which shows
  * that a wait that is never satisfied ends with a status the host can read

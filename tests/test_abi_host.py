@@ -124,8 +124,7 @@ def test_fused_dispatch_rejects_non_decode_shapes(lib):
     # beyond the single-cluster path (N*T <= 512, E <= 256) the cooperative
     # kernel's limits apply
     for kw, why in [(dict(N=4, T=4096, E=128, R=8, H=128), "4096"),
-                    (dict(N=4, T=200, E=16, R=2, H=128), "multiple of 32"),
-                    (dict(N=4, T=192, E=64, R=16, H=128), "R > 8"),
+                    (dict(N=4, T=192, E=64, R=17, H=128), "R > 16"),
                     (dict(N=4, T=64, E=1024, R=8, H=128), "E > 512")]:
         d = moe.make_dims(**kw)
         assert lib.moe_dispatch_fused(ctypes.byref(d), ok, None, 0, 0, ok, None, *args[:11], None,

@@ -1,7 +1,8 @@
-"""Parity of the decode-fused dispatch (route + count + pack in one
-cooperative launch) with the oracle; same bar as the separate calls:
-indices, counts, positions and packed rows bit-exact, weights within 2e-6,
-combine within the combine tolerance."""
+"""Parity of the decode-fused dispatch (route + count + pack in one launch:
+one thread-block cluster for small batches, else one cooperative launch)
+with the oracle; same bar as the separate calls: indices, counts, positions
+and packed rows bit-exact (and nothing written outside the occupied rows),
+weights within 2e-6, combine within the combine tolerance."""
 import numpy as np
 import pytest
 import torch
@@ -32,7 +33,7 @@ CASES = {
     # ties, sigmoid without renormalisation, a bias
     "ties_sigmoid": W.Workload("ties_sigmoid", N=8, T=32, E=64, R=6, H=256, score_fn=W.SIGMOID,
                                bias="normal", seed=61),
-    # one expert per rank, f32 rows, ragged last count block (N*T = 700 is not a multiple of 256)
+    # one expert per rank, f32 rows, N*T = 672 split unevenly over the blocks
     "f32_ragged": W.Workload("f32_ragged", N=7, T=96, E=14, R=2, H=72, x_dtype=W.F32,
                              y_dtype=W.F32, renormalize=True, seed=62),
     # fp8 rows with block scales
@@ -50,10 +51,26 @@ CASES = {
     "odd_e_small": W.Workload("odd_e_small", N=1, T=64, E=7, R=3, H=64, seed=69),
     "odd_e_coop": W.Workload("odd_e_coop", N=3, T=320, E=9, R=3, H=64, seed=70),
     # 256 tokens with 14 KB rows: too much row traffic for the cluster path, so
-    # the cooperative kernel runs with a single count block
-    "coop_one_count_block": W.Workload("coop_one_count_block", N=2, T=128, E=16, R=4, H=7168,
-                                       score_fn=W.SIGMOID, renormalize=True, bias="normal",
-                                       expert_op=W.EXPERT_SCALE, seed=71),
+    # the cooperative kernel runs with one token per block
+    "coop_one_token_blocks": W.Workload("coop_one_token_blocks", N=2, T=128, E=16, R=4, H=7168,
+                                        score_fn=W.SIGMOID, renormalize=True, bias="normal",
+                                        expert_op=W.EXPERT_SCALE, seed=71),
+    # cooperative kernel, T not a multiple of 32 (blocks straddle source ranks)
+    "coop_t100": W.Workload("coop_t100", N=8, T=100, E=64, R=6, H=256, renormalize=True,
+                            bias="normal", seed=74),
+    # cooperative kernel, R = 16 (512 pairs in a block of 32 tokens at most)
+    "coop_r16": W.Workload("coop_r16", N=4, T=160, E=64, R=16, H=128, score_fn=W.SIGMOID, seed=75),
+    # cooperative kernel, one token per rank and 512 ranks: blocks of one or
+    # two tokens, each from its own source rank
+    "coop_t1_n512": W.Workload("coop_t1_n512", N=512, T=1, E=512, R=4, H=64, bias="normal",
+                               seed=76),
+    # cooperative kernel at its largest batch with the widest expert table
+    # (4096 tokens, E = 512: 16 experts per lane)
+    "coop_4096_e512": W.Workload("coop_4096_e512", N=16, T=256, E=512, R=8, H=256,
+                                 score_fn=W.SIGMOID, renormalize=True, bias="normal", seed=77),
+    # cooperative kernel, capacity overflow
+    "coop_capacity": W.Workload("coop_capacity", N=8, T=96, E=32, R=4, H=128, cap_rows=300,
+                                seed=78),
     # shapes only the single-cluster path takes: one token per rank (T % 32
     # != 0) and R > 8
     "decode_t1": W.Workload("decode_t1", N=64, T=1, E=128, R=8, H=256, score_fn=W.SIGMOID,
@@ -72,14 +89,14 @@ def test_fused_cases(name):
     w = CASES[name]
     inp = W.make_inputs(w, tie_every=3 if name == "ties_sigmoid" else 0)
     gr, _, _ = _compare(w, inp, fused=True)
-    assert gr.status == (oracle.ERR_CAPACITY if name == "capacity" else oracle.OK)
+    assert gr.status == (oracle.ERR_CAPACITY if name in ("capacity", "coop_capacity") else oracle.OK)
 
 
-# dsv3_decode and past_small take the cooperative kernel; tiny and small_max
-# the single thread-block cluster (up to 512 tokens, E <= 256, at most 1 MB of
-# rows read and written per 32 tokens)
-@pytest.mark.parametrize("name", ["dsv3_decode", "past_small", "tiny", "small_max", "decode_t1",
-                                  "r12_t24"])
+# dsv3_decode, kimi_k2_decode, past_small and the coop_ cases take the
+# cooperative kernel; tiny and small_max the single thread-block cluster (up
+# to 512 tokens, E <= 256, at most 1 MB of rows read and written per 32 tokens)
+@pytest.mark.parametrize("name", ["dsv3_decode", "kimi_k2_decode", "past_small", "tiny", "small_max",
+                                  "decode_t1", "r12_t24", "coop_t100", "coop_r16", "coop_t1_n512"])
 def test_fused_equals_separate_calls_bytewise(name):
     w = W.WORKLOADS.get(name) or CASES[name]
     inp = W.make_inputs(w)
@@ -94,7 +111,7 @@ def test_fused_equals_separate_calls_bytewise(name):
 
 
 @pytest.mark.parametrize("static", [False, True])
-@pytest.mark.parametrize("R", [2, 16])  # R = 16 is past both fused kernels' limits
+@pytest.mark.parametrize("R", [2, 17])  # R = 17 is past both fused kernels' limits
 def test_fused_empty_batch(static, R):
     """N*T == 0 is always accepted: zero counts and offsets, MOE_OK, as the
     separate calls give."""

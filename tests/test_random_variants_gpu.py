@@ -53,8 +53,8 @@ def _fused_shapes(n, seed=31):
         while E > 512:
             E //= 2
         E = max(N, E // N * N)
-        R = rng.randint(1, min(E, 8))
-        T = 32 * rng.randint(1, max(1, min(8, 4096 // (32 * N))))
+        R = rng.randint(1, min(E, 16))
+        T = rng.randint(1, max(1, min(256, 4096 // N)))
         x_dtype, H, y_dtype, op = _rows(rng)
         score = rng.choice([W.SOFTMAX, W.SIGMOID]) | (FLAG if rng.random() < 0.25 else 0)
         cap = 0 if rng.random() < 0.8 else max(1, N * T * max(R, E // N) // 16)
