@@ -867,7 +867,8 @@ def variants_of(args, run, nb, host_lead, per_timed):
             run.launch("route")
             run.launch("count")
             qpack()
-        qm = run.timed_repeat(qpack, nb, host_lead)
+        with nvtx_range("pack_quant"):
+            qm = run.timed_repeat(qpack, nb, host_lead)
         cm = run.timed_repeat(chain, nb, host_lead)
         qbytes = w.NT * (2 * w.H + w.R * (w.H + 4 * (w.H // 128))) + w.NT * w.R * 8
         quant = {"ms": qm, "alg_bytes": qbytes, "alg_gbs": qbytes / (qm / 1e3) / 1e9,
@@ -881,7 +882,8 @@ def variants_of(args, run, nb, host_lead, per_timed):
 
     # decode-fused dispatch (route + count + pack in one launch) on the same
     # inputs, when the batch is a decode batch it supports
-    fused = run.fused_ms(nb, host_lead)
+    with nvtx_range("fused"):
+        fused = run.fused_ms(nb, host_lead)
     if "ms" in fused:
         fused.update({"vs_separate_dispatch_ms": per_timed["dispatch (route+count+pack)"],
                       "step_ms_if_used": fused["ms"] + per_timed["combine"],
@@ -912,6 +914,8 @@ def variants_of(args, run, nb, host_lead, per_timed):
     evs2 = []
     ppool = [new_events(3) for _ in range(nb + 3)]
     host_lead(nb + 3)
+    send_range = nvtx_range("send_side")
+    send_range.__enter__()
     for i in range(nb + 3):
         run.flush()
         e = ppool[i]
@@ -923,6 +927,7 @@ def variants_of(args, run, nb, host_lead, per_timed):
         if i >= 3:
             evs2.append(e)
     torch.cuda.synchronize(dev)
+    send_range.__exit__(None, None, None)
     used = int((slot_rank >= 0).sum().item())
     yb = W.y_row_bytes(w)
     t_part = statistics.mean(e[0].elapsed_time(e[1]) for e in evs2)
