@@ -5,6 +5,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <cuda.h>  // CUcontext and CUresult only: the two driver calls are fetched at run time
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -19,6 +21,38 @@ int set_error(int code, const char *fmt, ...) {
     vsnprintf(g_err, sizeof(g_err), fmt, ap);
     va_end(ap);
     return code;
+}
+
+namespace {
+// Driver functions fetched through the runtime (no link against libcuda).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+struct CtxFns {
+    CtxGetCurrentFn get_current = nullptr;
+    CtxGetIdFn get_id = nullptr;
+    CtxFns() {
+        cudaDriverEntryPointQueryResult q;
+        void *f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(f);
+        cudaGetLastError();
+    }
+};
+}  // namespace
+
+unsigned long long context_key() {
+    static const CtxFns fns;  // initialised once, thread-safe
+    if (fns.get_current == nullptr || fns.get_id == nullptr) return 0;
+    CUcontext ctx = nullptr;
+    if (fns.get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    unsigned long long id = 0;
+    if (fns.get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id + 1;  // never 0 for a real context
 }
 
 int sm_count() {

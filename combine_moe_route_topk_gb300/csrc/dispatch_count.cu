@@ -513,16 +513,18 @@ dispatch_count_kernel(const int32_t *__restrict__ topk_idx, int N, int T, int E,
 }
 
 // Largest cluster (<= 16 blocks) of this kernel with this much shared memory
-// that the current device can co-schedule; 0 if none.  Cached per host thread
-// and device for the largest shared-memory request seen.
+// that the current device can co-schedule; 0 if none.  Cached per host
+// thread, device and context for the largest shared-memory request seen.
 template <int kThreads, int kMaxR>
 int max_cluster_blocks(size_t smem_bytes) {
     static thread_local int cached_dev = -1;
+    static thread_local unsigned long long cached_ctx = 0;
     static thread_local size_t cached_smem = 0;
     static thread_local int cached_c = 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (dev == cached_dev && smem_bytes <= cached_smem) return cached_c;
+    const unsigned long long ctx = context_key();
+    if (dev == cached_dev && ctx != 0 && ctx == cached_ctx && smem_bytes <= cached_smem) return cached_c;
     auto kern = dispatch_count_kernel<kThreads, kMaxR>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes) !=
         cudaSuccess)
@@ -550,6 +552,7 @@ int max_cluster_blocks(size_t smem_bytes) {
         cudaGetLastError();
     }
     cached_dev = dev;
+    cached_ctx = context_key();  // the attribute calls above created the context if needed
     cached_smem = smem_bytes;
     cached_c = best;
     return best;

@@ -47,8 +47,6 @@
 // anything else with MOE_ERR_UNSUPPORTED (use the three separate calls).
 #include <mutex>
 
-#include <cuda.h>  // CUcontext and CUresult only: the two driver calls are fetched at run time
-
 #include "mem_ops.cuh"
 #include "moe_internal.cuh"
 #include "pdl.cuh"
@@ -550,34 +548,6 @@ struct ScratchEntry {
 };
 ScratchEntry g_scratch[kMaxScratchDevices] = {};
 
-// Driver functions fetched through the runtime (no link against libcuda).
-typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
-typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
-CtxGetCurrentFn g_ctx_get_current = nullptr;
-CtxGetIdFn g_ctx_get_id = nullptr;
-bool g_driver_fns_looked_up = false;
-
-// Unique id of the calling thread's current context; false if there is
-// none yet or the driver cannot say.
-bool current_context_id(unsigned long long *id) {
-    if (!g_driver_fns_looked_up) {
-        g_driver_fns_looked_up = true;
-        cudaDriverEntryPointQueryResult q;
-        void *f = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess && q == cudaDriverEntryPointSuccess)
-            g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f);
-        f = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f);
-        cudaGetLastError();
-    }
-    if (g_ctx_get_current == nullptr || g_ctx_get_id == nullptr) return false;
-    CUcontext ctx = nullptr;
-    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
-    return g_ctx_get_id(ctx, id) == CUDA_SUCCESS;
-}
 }  // namespace
 
 int64_t fused_static_scratch_bytes() { return kStaticScratchBytes; }
@@ -593,16 +563,16 @@ cudaError_t fused_static_scratch(void **out) {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxScratchDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    unsigned long long id = 0;
-    const bool have_id = current_context_id(&id);
-    if (have_id && g_scratch[dev].addr != nullptr && g_scratch[dev].ctx_id == id) {
+    const unsigned long long id = context_key();
+    if (id != 0 && g_scratch[dev].addr != nullptr && g_scratch[dev].ctx_id == id) {
         *out = g_scratch[dev].addr;
         return cudaSuccess;
     }
     void *p = nullptr;
     e = cudaGetSymbolAddress(&p, g_fused_static_scratch);  // creates the context if needed
     if (e != cudaSuccess) return e;
-    if (current_context_id(&id)) g_scratch[dev] = ScratchEntry{p, id};
+    const unsigned long long id2 = context_key();
+    if (id2 != 0) g_scratch[dev] = ScratchEntry{p, id2};
     *out = p;
     return cudaSuccess;
 }

@@ -185,17 +185,20 @@ cudaError_t launch_dispatch_pack_bulk(const void *x, const float *x_scales, cons
     if (stages == 0) return cudaErrorInvalidValue;
     const size_t smem = (size_t)stages * (size_t)row_bytes;
     // the attribute belongs to the current device's context: cached per
-    // host thread and device
+    // host thread, device and context
     static thread_local int configured_dev = -1;
+    static thread_local unsigned long long configured_ctx = 0;
     static thread_local size_t configured = 0;
     int dev = 0;
     cudaError_t de = cudaGetDevice(&dev);
     if (de != cudaSuccess) return de;
-    if (dev != configured_dev || smem > configured) {
+    const unsigned long long ctx = context_key();
+    if (dev != configured_dev || ctx == 0 || ctx != configured_ctx || smem > configured) {
         cudaError_t e = cudaFuncSetAttribute(dispatch_pack_bulk_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured_dev = dev;
+        configured_ctx = context_key();
         configured = smem;
     }
     int per_sm = 0;

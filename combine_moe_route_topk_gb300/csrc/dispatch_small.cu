@@ -258,13 +258,15 @@ cudaError_t launch_small_jv(const SmallParams &P, int C, cudaStream_t stream) {
     attr[1] = pdl_attribute();
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    // the cluster must fit the device: checked once per host thread, device
-    // and cluster size reached so far
+    // the cluster must fit the device: checked once per host thread, device,
+    // context and cluster size reached so far
     static thread_local int ok_dev = -1, ok_c = 0;
+    static thread_local unsigned long long ok_ctx = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev != ok_dev || C > ok_c) {
+    const unsigned long long ctx = context_key();
+    if (dev != ok_dev || ctx == 0 || ctx != ok_ctx || C > ok_c) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
         int n = 0;
@@ -274,8 +276,9 @@ cudaError_t launch_small_jv(const SmallParams &P, int C, cudaStream_t stream) {
             return cudaErrorNotSupported;
         }
         cfg.numAttrs = 2;
-        if (dev != ok_dev) ok_c = 0;
+        if (dev != ok_dev || ctx != ok_ctx) ok_c = 0;
         ok_dev = dev;
+        ok_ctx = context_key();
         ok_c = C > ok_c ? C : ok_c;
     }
     return cudaLaunchKernelEx(&cfg, kern, P);

@@ -12,6 +12,12 @@ namespace moe {
 // Sets the calling thread's message for moe_last_error(); returns `code`.
 int set_error(int code, const char *fmt, ...);
 
+// Unique key of the calling thread's current CUDA context (0 if there is
+// none yet or the driver cannot say).  Host-side caches of per-context state
+// (kernel attributes, symbol addresses) key on it as well as on the device,
+// because cudaDeviceReset ends the context and the next call gets a new one.
+unsigned long long context_key();
+
 // Multiprocessor count of the current device (cached per device).
 int sm_count();
 int64_t l2_bytes();  // L2 cache size of the current device (0 if unknown)
