@@ -135,3 +135,53 @@ def test_fused_empty_batch(static, R):
     assert moe.read_status(b.status) == moe.MOE_OK
     for t in (b.expert_counts, b.expert_offsets, b.rank_counts, b.rank_offsets, b.send_counts):
         assert int(t.abs().sum()) == 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "dsv3_decode"])
+def test_fused_dispatch_captures_into_a_cuda_graph(name):
+    """moe_dispatch_fused enqueues only stream work with fixed shapes (the
+    single-cluster kernel, or a memset, the cooperative route-count kernel
+    and the pack kernel), so it captures into a CUDA graph; a replay on new
+    inputs gives the oracle's routing, counts, positions and rows."""
+    w = W.WORKLOADS[name]
+    dims = moe.dims_of(w)
+    b = moe.Buffers(dims)
+    inp = W.make_inputs(w, device="cuda")
+    logits, x = inp.logits.clone(), inp.x.clone()
+    bias = None if inp.bias is None else inp.bias.clone()
+    ws = torch.empty(b.sizes["fused_workspace_bytes"], dtype=torch.uint8, device="cuda")
+
+    def call():
+        moe.dispatch_fused(dims, logits, bias, w.score_fn, w.renormalize, x, None, b.topk_idx,
+                           b.topk_w, b.expert_counts, b.expert_offsets, b.rank_counts,
+                           b.rank_offsets, b.send_counts, b.pos, b.status, b.packed_x, None,
+                           b.packed_src, ws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()  # warm-up outside the capture (sets kernel attributes)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    w2 = w.replace(seed=w.seed + 7)
+    inp2 = W.make_inputs(w2)
+    logits.copy_(inp2.logits)
+    x.copy_(inp2.x)
+    if bias is not None:
+        bias.copy_(inp2.bias)
+    b.pos.fill_(-5)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert moe.read_status(b.status) == moe.MOE_OK
+    ref = oracle.run(w2, inp2, with_combine=False)
+    np.testing.assert_array_equal(b.topk_idx.cpu().numpy(), ref["topk_idx"])
+    np.testing.assert_allclose(b.topk_w.cpu().numpy(), ref["topk_w"], rtol=2e-6, atol=0)
+    for k in ("expert_counts", "expert_offsets", "rank_counts", "rank_offsets", "send_counts", "pos"):
+        np.testing.assert_array_equal(getattr(b, k).cpu().numpy(), ref[k], err_msg=k)
+    pos = ref["pos"].ravel()
+    pos = pos[pos >= 0]
+    crow = ref["rank_offsets"][pos // ref["cap"]] + pos % ref["cap"]
+    got = oracle.x_as_bytes(b.packed_x[torch.from_numpy(pos).long().cuda()].cpu())
+    np.testing.assert_array_equal(got, ref["packed_x"][crow])
