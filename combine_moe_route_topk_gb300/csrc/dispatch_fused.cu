@@ -67,10 +67,10 @@ constexpr int kCMaxNT = 4096;
 constexpr int kSendSmem = 2048;                // ints of send-count staging per block
 constexpr long long kSpinLimit = 1ll << 20;    // polls of the release wait (well under a second)
 
-// workspace: words of the arrival counter, generation, error and overflow
-// flag in separate 128-byte lines, then the byte histograms, the chunk
-// prefixes (u16) and the expert offsets
-constexpr int kWsArrive = 0, kWsGen = 32, kWsError = 64, kWsOver = 96;
+// workspace: words of the arrival counter, generation and error flag in
+// separate 128-byte lines, then the byte histograms, the chunk prefixes
+// (u16) and the expert offsets
+constexpr int kWsArrive = 0, kWsGen = 32, kWsError = 64;
 constexpr int kWsHeaderBytes = 512;
 
 __host__ __device__ inline int pad16(int v) { return (v + 15) & ~15; }
@@ -298,7 +298,6 @@ route_count_kernel(FusedParams P) {
         if (tid == 0) {
             P.rank_offsets[N] = tot[E];
             *P.status = over ? MOE_ERR_CAPACITY : MOE_OK;
-            ws_words[kWsOver] = over;
         }
         __syncthreads();  // every thread's prefixes, offsets and zeroed send counts
         if (tid == 0) {
@@ -360,11 +359,27 @@ template <int J, bool kVec4>
 cudaError_t launch_fused_jv(FusedParams P, cudaStream_t stream) {
     auto kern = route_count_kernel<J, kVec4>;
     const size_t smem = (size_t)coop_smem_layout(P.E).bytes;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // the shared-memory attribute and the occupancy it allows belong to the
+    // current context: cached per host thread, device and context for the
+    // largest request seen
+    static thread_local int cached_dev = -1, cached_per_sm = 0;
+    static thread_local unsigned long long cached_ctx = 0;
+    static thread_local size_t cached_smem = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCThreads, smem);
-    if (e != cudaSuccess) return e;
+    const unsigned long long ctx = context_key();
+    int per_sm = cached_per_sm;
+    if (dev != cached_dev || ctx == 0 || ctx != cached_ctx || smem > cached_smem) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCThreads, smem);
+        if (e != cudaSuccess) return e;
+        cached_dev = dev;
+        cached_ctx = context_key();
+        cached_smem = smem;
+        cached_per_sm = per_sm;
+    }
     const int sms = sm_count();
     if (per_sm < 1 || sms < 1) return cudaErrorNotSupported;
     const int NT = P.N * P.T;

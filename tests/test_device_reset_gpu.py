@@ -6,8 +6,9 @@ those attributes are unset; the caches key on the context, so calls after a
 reset set them again.  This runs in a child process that uses the C ABI and
 the CUDA runtime through ctypes only (PyTorch's allocator does not survive a
 device reset): the count of a 5120-token batch with E = 512 (1024-thread
-blocks, about 96 KB of shared memory) and the single-cluster fused dispatch
-of a small batch, before and after a reset, with identical outputs."""
+blocks, about 96 KB of shared memory) and the fused dispatch of a 256-token
+batch (single cluster) and a 1024-token batch (cooperative route-count
+kernel), before and after a reset, with identical outputs."""
 import os
 import subprocess
 import sys
@@ -65,8 +66,10 @@ def count_round():
         rt.cudaFree(p)
     return pos, ec
 
-def fused_small_round():
-    N, T, E, R, H = 4, 64, 32, 4, 64
+def fused_round(T):
+    # T = 64: 256 tokens, the single-cluster kernel; T = 256: 1024 tokens,
+    # the cooperative route-count kernel and the pack kernel
+    N, E, R, H = 4, 32, 4, 64
     NT = N * T
     logits = rng.standard_normal((NT, E)).astype(np.float32)
     x = rng.integers(0, 1 << 16, (NT, H), dtype=np.uint16)
@@ -74,6 +77,7 @@ def fused_small_round():
     cap = N * T * max(R, E // N)
     sizes = dict(lg=logits.nbytes, x=x.nbytes, ti=4 * NT * R, tw=4 * NT * R, ec=4 * E, eo=4 * (E + 1), rc=4 * N,
                  ro=4 * (N + 1), sc=4 * N * N, pos=4 * NT * R, st=4, px=2 * H * N * cap, ps=4 * N * cap, ws=1 << 20)
+    st = np.empty(1, np.int32)
     b = {k: dmalloc(n) for k, n in sizes.items()}
     h2d(b["lg"], logits)
     h2d(b["x"], x)
@@ -84,6 +88,8 @@ def fused_small_round():
     assert rt.cudaDeviceSynchronize() == 0
     pos = np.empty((NT, R), np.int32)
     d2h(pos, b["pos"])
+    d2h(st, b["st"])
+    assert int(st[0]) == 0, int(st[0])
     for p in b.values():
         rt.cudaFree(p)
     return pos
@@ -91,12 +97,13 @@ def fused_small_round():
 lib.moe_last_error.restype = ctypes.c_char_p
 rng = np.random.default_rng(5)
 a_pos, a_ec = count_round()
-a_small = fused_small_round()
+a_small, a_coop = fused_round(64), fused_round(256)
 assert rt.cudaDeviceReset() == 0
 rng = np.random.default_rng(5)
 b_pos, b_ec = count_round()
-b_small = fused_small_round()
-assert (a_pos == b_pos).all() and (a_ec == b_ec).all() and (a_small == b_small).all()
+b_small, b_coop = fused_round(64), fused_round(256)
+assert (a_pos == b_pos).all() and (a_ec == b_ec).all()
+assert (a_small == b_small).all() and (a_coop == b_coop).all()
 assert int(a_ec.sum()) == 4 * 1280 * 8
 print("RESET_OK")
 '''
