@@ -470,7 +470,7 @@ class PathRunner:
         import torch
         moe, w, b, inp, dims = self.moe, self.w, self.b, self.inp, self.dims
         try:
-            ws = torch.empty(moe.buffer_sizes(dims)["fused_workspace_bytes"], dtype=torch.uint8,
+            ws = torch.zeros(moe.buffer_sizes(dims)["fused_workspace_bytes"], dtype=torch.uint8,
                              device=self.dev)
 
             def call():
@@ -888,7 +888,8 @@ def variants_of(args, run, nb, host_lead, per_timed):
         fused.update({"vs_separate_dispatch_ms": per_timed["dispatch (route+count+pack)"],
                       "step_ms_if_used": fused["ms"] + per_timed["combine"],
                       "note": "moe_dispatch_fused on the same batch (one thread-block cluster "
-                              "for batches of up to 512 tokens, else one cooperative launch)"})
+                              "for batches of up to 512 tokens, else a route kernel that also "
+                              "counts, then the pack kernel deriving the rows)"})
     out["fused_dispatch"] = fused
 
     # the router with the bias in the selection key only (score of the raw

@@ -201,7 +201,7 @@ int moe_buffer_sizes(const MoeDims *dims, MoeSizes *out) {
     out->partial_slots = dims->R < N ? dims->R : N;
     out->partial_bytes = v.NT * out->partial_slots * v.y_row_bytes;
     out->slot_rank_bytes = v.NT * out->partial_slots * 4;
-    out->fused_workspace_bytes = fused_workspace_bytes(dims->E);
+    out->fused_workspace_bytes = fused_workspace_bytes(dims->N, dims->T, dims->E);
     (void)H;
     return MOE_OK;
 }
@@ -426,9 +426,9 @@ int moe_dispatch_fused(const MoeDims *dims, const float *logits, const float *bi
                                           rank_offsets, send_counts, pos, status, packed_x,
                                           fp8 ? packed_scales : nullptr, packed_src, workspace,
                                           (cudaStream_t)stream);
-    if (e == cudaErrorNotSupported || e == cudaErrorCooperativeLaunchTooLarge)
+    if (e == cudaErrorNotSupported)
         return set_error(MOE_ERR_UNSUPPORTED, "moe_dispatch_fused: the device cannot run this batch fused "
-                                              "(cluster or co-resident blocks unavailable)");
+                                              "(thread-block cluster unavailable)");
     return cuda_result(e, "moe_dispatch_fused");
 }
 
@@ -444,11 +444,12 @@ int moe_dispatch_fused_static(const MoeDims *dims, const float *logits, const fl
     const char *why = fused_unsupported(dims->N, dims->T, dims->E, dims->R, v.x_row_bytes);
     if (why[0] != '\0')
         return set_error(MOE_ERR_UNSUPPORTED, "moe_dispatch_fused_static: %s; use the separate calls", why);
-    const int64_t need = fused_workspace_bytes(dims->E);
+    const int64_t need = fused_workspace_bytes(dims->N, dims->T, dims->E);
     if (v.NT > 0 && need > fused_static_scratch_bytes())  // an empty batch uses no scratch
         return set_error(MOE_ERR_UNSUPPORTED,
-                         "moe_dispatch_fused_static: E=%d needs %lld bytes of scratch; the library's static "
-                         "array holds %lld", dims->E, (long long)need, (long long)fused_static_scratch_bytes());
+                         "moe_dispatch_fused_static: N=%d T=%d E=%d needs %lld bytes of scratch; the library's "
+                         "static array holds %lld", dims->N, dims->T, dims->E, (long long)need,
+                         (long long)fused_static_scratch_bytes());
     void *scratch = nullptr;
     cudaError_t e = fused_static_scratch(&scratch);
     if (e != cudaSuccess) return cuda_result(e, "moe_dispatch_fused_static: scratch address");

@@ -25,6 +25,10 @@
 // (evict-last) before they wait for count; the R-fold row stores carry an
 // evict-first hint so that they do not push those rows out again.  The
 // prefetch covers at most half of the L2.
+//
+// The decode-fused dispatch launches the same kernel in a second form that
+// computes each pair's row itself from the per-block ranks and prefixes of
+// the fused route kernel (PackDerive) and writes it to pos.
 #include "mem_ops.cuh"
 #include "moe_internal.cuh"
 #include "pdl.cuh"
@@ -35,6 +39,46 @@ namespace {
 constexpr int kPackVecs = 2;          // 16-byte vectors of a row per thread
 constexpr int kPackMaxThreads = 1024;
 
+// Copies token g's row (and its fp8 scales) to the rows sp[0..R) (< 0:
+// dropped); the block's threads each move two 16-byte vectors at a time,
+// loads first, then the R stores.
+__device__ __forceinline__ void copy_token(const uint4 *__restrict__ x, const float *__restrict__ x_scales,
+                                           int64_t g, const int *sp, int R, int nvec, int spr,
+                                           uint4 *__restrict__ packed_x, float *__restrict__ packed_scales,
+                                           uint64_t stream_out) {
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    bool any = false;  // a token whose pairs were all dropped is not read
+    for (int k = 0; k < R; ++k) any |= sp[k] >= 0;
+    const uint4 *src = x + g * nvec;
+    for (int c0 = tid; any && c0 < nvec; c0 += nthr * kPackVecs) {
+        uint4 v[kPackVecs];
+#pragma unroll
+        for (int u = 0; u < kPackVecs; ++u) {
+            const int c = c0 + u * nthr;
+            if (c < nvec) v[u] = ld_stream(src + c);
+        }
+        for (int k = 0; k < R; ++k) {
+            const int p = sp[k];
+            if (p < 0) continue;
+            uint4 *dst = packed_x + (int64_t)p * nvec;
+#pragma unroll
+            for (int u = 0; u < kPackVecs; ++u) {
+                const int c = c0 + u * nthr;
+                if (c < nvec) st_evict_first(dst + c, v[u], stream_out);
+            }
+        }
+    }
+    if (spr > 0) {
+        for (int i = tid; i < R * spr; i += nthr) {
+            const int k = i / spr, j = i - k * spr;
+            const int p = sp[k];
+            if (p >= 0) packed_scales[(int64_t)p * spr + j] = __ldg(x_scales + g * spr + j);
+        }
+    }
+}
+
+// The pack kernel: pos[g][k] is the row of pair (g, k), written by the
+// count kernel.  One token per block step.
 __global__ void __launch_bounds__(kPackMaxThreads)
 dispatch_pack_kernel(const uint4 *__restrict__ x, const float *__restrict__ x_scales,
                      const int32_t *__restrict__ pos, int64_t NT, int R, int nvec, int spr,
@@ -42,7 +86,7 @@ dispatch_pack_kernel(const uint4 *__restrict__ x, const float *__restrict__ x_sc
                      uint4 *__restrict__ packed_x, float *__restrict__ packed_scales,
                      int32_t *__restrict__ packed_src) {
     __shared__ int s_pos[32];
-    const int tid = threadIdx.x, nthr = blockDim.x;  // nthr >= 32 >= R
+    const int tid = threadIdx.x;  // blockDim.x >= 32 >= R
     prefetch_rows_l2(x, (int64_t)nvec * 16, pf_rows, pf_blocks);  // before the wait: hints only
     grid_dependency_wait();  // pos comes from the count kernel (x may come from earlier ones)
     grid_launch_dependents();
@@ -55,56 +99,98 @@ dispatch_pack_kernel(const uint4 *__restrict__ x, const float *__restrict__ x_sc
             if (ok) packed_src[p] = (int32_t)(g * R + tid);
         }
         __syncthreads();
-        bool any = false;  // a token whose pairs were all dropped is not read
-        for (int k = 0; k < R; ++k) any |= s_pos[k] >= 0;
-        const uint4 *src = x + g * nvec;
-        for (int c0 = tid; any && c0 < nvec; c0 += nthr * kPackVecs) {
-            uint4 v[kPackVecs];
-#pragma unroll
-            for (int u = 0; u < kPackVecs; ++u) {
-                const int c = c0 + u * nthr;
-                if (c < nvec) v[u] = ld_stream(src + c);
-            }
-            for (int k = 0; k < R; ++k) {
-                const int p = s_pos[k];
-                if (p < 0) continue;
-                uint4 *dst = packed_x + (int64_t)p * nvec;
-#pragma unroll
-                for (int u = 0; u < kPackVecs; ++u) {
-                    const int c = c0 + u * nthr;
-                    if (c < nvec) st_evict_first(dst + c, v[u], stream_out);
-                }
-            }
-        }
-        if (spr > 0) {
-            for (int i = tid; i < R * spr; i += nthr) {
-                const int k = i / spr, j = i - k * spr;
-                const int p = s_pos[k];
-                if (p >= 0) packed_scales[(int64_t)p * spr + j] = __ldg(x_scales + g * spr + j);
-            }
-        }
+        copy_token(x, x_scales, g, s_pos, R, nvec, spr, packed_x, packed_scales, stream_out);
         __syncthreads();  // s_pos is rewritten for the next token
     }
 }
 
-}  // namespace
+// The deriving form (the decode-fused dispatch, see PackDerive): each pair's
+// row is computed here and written to pos.  It takes two tokens per block
+// step and derives the rows of both before copying either, so its extra
+// dependent round trip to L2 is paid once per two tokens; held to 32
+// registers, like the plain form, so that as many blocks share an SM.
+__global__ void __launch_bounds__(kPackMaxThreads, 2)
+dispatch_pack_derive_kernel(const uint4 *__restrict__ x, const float *__restrict__ x_scales,
+                            int32_t *pos, int64_t NT, int R, int nvec, int spr,
+                            int64_t rows_total, int64_t pf_rows, int pf_blocks, PackDerive D,
+                            uint4 *__restrict__ packed_x, float *__restrict__ packed_scales,
+                            int32_t *__restrict__ packed_src) {
+    constexpr int kTok = 2;
+    __shared__ int s_pos[kTok * 32];
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    prefetch_rows_l2(x, (int64_t)nvec * 16, pf_rows, pf_blocks);  // before the wait: hints only
+    grid_dependency_wait();  // ranks and prefixes come from the fused route kernel
+    grid_launch_dependents();
+    if (D.blocks_per_rank > 0 && (int)blockIdx.x < D.N) {
+        // row s of send_counts: the counts of the blocks of source rank s
+        const int s = (int)blockIdx.x, cps = D.blocks_per_rank;
+        for (int d = tid; d < D.N; d += nthr) {
+            int c = 0;
+            for (int k = 0; k < cps; ++k) c += __ldg(D.block_send + (int64_t)(s * cps + k) * D.N + d);
+            D.send_counts[(int64_t)s * D.N + d] = c;
+        }
+    }
+    const uint64_t stream_out = l2_policy_evict_first();
+    for (int64_t g0 = (int64_t)blockIdx.x * kTok; g0 < NT; g0 += (int64_t)gridDim.x * kTok) {
+        for (int i = tid; i < kTok * R; i += nthr) {
+            const int u = i / R, k = i - u * R;
+            const int64_t g = g0 + u;
+            int p = -1;
+            if (g < NT) {
+                // row = d*cap + (start of expert e within rank d) + pairs of e in
+                // earlier chunks and earlier blocks of this chunk + rank among
+                // this block's pairs of e
+                const int e = __ldg(D.topk_idx + g * R + k);
+                const int r = pos[g * R + k];
+                const int gi = (int)g;
+                const int b = D.ranks_per_block > 0 ? gi / (D.ranks_per_block * D.T)
+                                                    : (gi / D.T) * D.blocks_per_rank + (gi % D.T) / 32;
+                const int d = e / D.L;
+                const int c0 = b & ~7;  // first block of b's chunk of 8
+                int local = __ldg(D.expert_offsets + e) - __ldg(D.expert_offsets + d * D.L) +
+                            (int)__ldg(D.chunk_prefix + (int64_t)(b >> 3) * D.Ep + e) + r;
+#pragma unroll
+                for (int j = 0; j < 7; ++j)
+                    if (c0 + j < b) local += __ldg(D.block_hist + (int64_t)(c0 + j) * D.Ep + e);
+                p = local < D.cap ? d * D.cap + local : -1;
+                pos[g * R + k] = p;
+                if (p >= 0 && (int64_t)p < rows_total) packed_src[p] = (int32_t)(g * R + k);
+                else p = -1;
+            }
+            s_pos[i] = p;
+        }
+        __syncthreads();
+        for (int u = 0; u < kTok && g0 + u < NT; ++u)
+            copy_token(x, x_scales, g0 + u, s_pos + u * R, R, nvec, spr, packed_x, packed_scales, stream_out);
+        __syncthreads();  // s_pos is rewritten for the next tokens
+    }
+}
 
-cudaError_t launch_dispatch_pack(const void *x, const float *x_scales, const int32_t *pos,
-                                 int64_t NT, int R, int64_t row_bytes, int scales_per_row,
-                                 int64_t rows_total, void *packed_x,
-                                 float *packed_scales, int32_t *packed_src, cudaStream_t stream) {
+// Grid, block and prefetch shape shared by both forms.
+template <bool kDerive>
+cudaError_t launch_pack(const void *x, const float *x_scales, int32_t *pos, int64_t NT, int R,
+                        int64_t row_bytes, int scales_per_row, int64_t rows_total, bool prefetch,
+                        const PackDerive &D, void *packed_x, float *packed_scales,
+                        int32_t *packed_src, cudaStream_t stream) {
     if (NT == 0) return cudaSuccess;
     const int nvec = (int)(row_bytes / 16);
-    const int64_t grid = NT < (int64_t)0x7fffffff ? NT : (int64_t)0x7fffffff;
+    const int64_t steps = kDerive ? (NT + 1) / 2 : NT;  // the deriving form takes two tokens per step
+    const int64_t grid = steps < (int64_t)0x7fffffff ? steps : (int64_t)0x7fffffff;
     // threads: two vectors of the row each, a whole number of warps (>= 32,
     // which also covers the R <= 32 position loads), at most 1024
     int64_t threads = ((nvec + kPackVecs - 1) / kPackVecs + 31) / 32 * 32;
     if (threads < 32) threads = 32;
     if (threads > kPackMaxThreads) threads = kPackMaxThreads;
     // prefetch: rows filling at most half the L2, issued by one block per SM
-    int64_t pf_rows = row_bytes <= 65536 ? (l2_bytes() / 2) / row_bytes : 0;
-    if (pf_rows > NT) pf_rows = NT;
+    // or, in the deriving form, by the blocks that fit beside the fused
+    // route kernel (its blocks of 1024 threads fill the SMs they run on)
+    int64_t pf_rows = prefetch ? pack_prefetch_rows(NT, row_bytes) : 0;
     int64_t pf_blocks = sm_count();
+    if (kDerive && D.route_blocks < pf_blocks) {
+        int64_t per_sm = 2048 / threads;
+        if (per_sm > 32) per_sm = 32;
+        pf_blocks = (pf_blocks - D.route_blocks) * per_sm;
+    }
     if (pf_blocks > grid) pf_blocks = grid;
     if (pf_rows <= 0 || pf_blocks <= 0) pf_rows = pf_blocks = 0;
     cudaLaunchConfig_t cfg = {};
@@ -114,10 +200,40 @@ cudaError_t launch_dispatch_pack(const void *x, const float *x_scales, const int
     cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, dispatch_pack_kernel, reinterpret_cast<const uint4 *>(x),
-                              x_scales, pos, NT, R, nvec, scales_per_row, rows_total,
-                              pf_rows, (int)pf_blocks, reinterpret_cast<uint4 *>(packed_x),
-                              packed_scales, packed_src);
+    if constexpr (kDerive)
+        return cudaLaunchKernelEx(&cfg, dispatch_pack_derive_kernel, reinterpret_cast<const uint4 *>(x),
+                                  x_scales, pos, NT, R, nvec, scales_per_row, rows_total, pf_rows,
+                                  (int)pf_blocks, D, reinterpret_cast<uint4 *>(packed_x), packed_scales,
+                                  packed_src);
+    else
+        return cudaLaunchKernelEx(&cfg, dispatch_pack_kernel, reinterpret_cast<const uint4 *>(x), x_scales,
+                                  static_cast<const int32_t *>(pos), NT, R, nvec, scales_per_row, rows_total,
+                                  pf_rows, (int)pf_blocks, reinterpret_cast<uint4 *>(packed_x),
+                                  packed_scales, packed_src);
+}
+
+}  // namespace
+
+int64_t pack_prefetch_rows(int64_t NT, int64_t row_bytes) {
+    int64_t rows = row_bytes <= 65536 ? (l2_bytes() / 2) / row_bytes : 0;
+    return rows < NT ? rows : NT;
+}
+
+cudaError_t launch_dispatch_pack(const void *x, const float *x_scales, const int32_t *pos,
+                                 int64_t NT, int R, int64_t row_bytes, int scales_per_row,
+                                 int64_t rows_total, void *packed_x,
+                                 float *packed_scales, int32_t *packed_src, cudaStream_t stream) {
+    // pos is only read in this form
+    return launch_pack<false>(x, x_scales, const_cast<int32_t *>(pos), NT, R, row_bytes, scales_per_row,
+                              rows_total, true, PackDerive{}, packed_x, packed_scales, packed_src, stream);
+}
+
+cudaError_t launch_dispatch_pack_derive(const void *x, const float *x_scales, int32_t *pos, int64_t NT,
+                                        int R, int64_t row_bytes, int scales_per_row, int64_t rows_total,
+                                        const PackDerive &D, void *packed_x, float *packed_scales,
+                                        int32_t *packed_src, cudaStream_t stream) {
+    return launch_pack<true>(x, x_scales, pos, NT, R, row_bytes, scales_per_row, rows_total, true, D,
+                             packed_x, packed_scales, packed_src, stream);
 }
 
 }  // namespace moe

@@ -40,6 +40,36 @@ cudaError_t launch_dispatch_pack(const void *x, const float *x_scales, const int
                                  int64_t rows_total, void *packed_x, float *packed_scales,
                                  int32_t *packed_src, cudaStream_t stream);
 
+// Pack whose positions are derived from per-block ranks (the second kernel
+// of the decode-fused dispatch).  Token g lies in block b of the fused
+// route kernel: b = g / (ranks_per_block * T) when blocks hold whole source
+// ranks (ranks_per_block > 0), else (g / T) * blocks_per_rank + (g % T) / 32.
+// On entry pos[g][k] holds the pair's rank among block b's pairs of its
+// expert e = topk_idx[g][k]; the kernel replaces it with the row
+//   local = expert_offsets[e] - expert_offsets[d*L] + chunk_prefix[(b/8)*Ep + e]
+//           + sum over b' in [8*(b/8), b) of block_hist[b'*Ep + e] + rank,
+//   pos   = local < cap ? d*cap + local : -1          (d = e / L)
+// and packs as launch_dispatch_pack does.  When source ranks are split over
+// several blocks (blocks_per_rank > 0), block s < N of the pack kernel also
+// writes row s of send_counts, the sum of the per-block counts block_send.
+struct PackDerive {
+    const int32_t *topk_idx;
+    const int32_t *expert_offsets;
+    const uint16_t *chunk_prefix;  // [blocks/8][Ep]: pairs of expert e in chunks of 8 blocks before
+    const unsigned char *block_hist;  // [blocks][Ep]: pairs of expert e in block b
+    const uint16_t *block_send;    // [blocks][N]: pairs of block b sent to rank d
+    int32_t *send_counts;
+    int N, T, ranks_per_block, blocks_per_rank, L, Ep, cap;
+    int route_blocks;  // blocks of the fused route kernel (each fills an SM)
+};
+cudaError_t launch_dispatch_pack_derive(const void *x, const float *x_scales, int32_t *pos, int64_t NT,
+                                        int R, int64_t row_bytes, int scales_per_row, int64_t rows_total,
+                                        const PackDerive &D, void *packed_x, float *packed_scales,
+                                        int32_t *packed_src, cudaStream_t stream);
+// Rows of x the pack prefetches into L2 (at most half the L2; 0 for rows
+// wider than one bulk prefetch).
+int64_t pack_prefetch_rows(int64_t NT, int64_t row_bytes);
+
 // Bulk-copy pack (whole rows through shared memory); rows of more than
 // 48 KB are not supported (pack_bulk_stages returns 0).
 int pack_bulk_stages(int64_t row_bytes);
@@ -52,8 +82,9 @@ cudaError_t launch_dispatch_pack_bulk(const void *x, const float *x_scales, cons
 // wait inside a kernel gives up).
 cudaError_t take_device_error(int *err, cudaStream_t stream);
 
-// Decode-fused route + count + pack (one cooperative launch).
-int64_t fused_workspace_bytes(int E);
+// Decode-fused route + count + pack.  Workspace bytes for a batch (0 when
+// no fused form that uses a workspace takes it).
+int64_t fused_workspace_bytes(int N, int T, int E);
 const char *fused_unsupported(int N, int T, int E, int R, int64_t row_bytes);  // "" when supported
 cudaError_t launch_dispatch_fused(const float *logits, const float *bias, int score_fn, int renormalize,
                                   const void *x, const float *x_scales, int N, int T, int E, int R,

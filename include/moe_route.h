@@ -45,7 +45,10 @@
  *   - MoeDims.reserved makes the padding before the 64-bit cap_rows explicit
  *     (the same layout under every compiler and binding); it must be 0.
  *   - The device status word also reports invalid expert ids
- *     (MOE_ERR_INVALID_ARG) and bounded waits that gave up (MOE_ERR_TIMEOUT).
+ *     (MOE_ERR_INVALID_ARG).  MOE_ERR_TIMEOUT, reserved in the problem
+ *     statement, reports a bounded wait that gave up (the bulk pack's
+ *     shared-memory barriers, through moe_take_device_error; the wait
+ *     self-test, through its status word).
  */
 #ifndef MOE_ROUTE_H
 #define MOE_ROUTE_H
@@ -62,7 +65,7 @@ extern "C" {
 #define MOE_ERR_UNSUPPORTED (-2) /* valid request this build does not implement */
 #define MOE_ERR_CUDA (-3)        /* a CUDA runtime call or kernel launch failed */
 #define MOE_ERR_CAPACITY (-4)    /* device status: a rank received more than cap_rows rows */
-#define MOE_ERR_TIMEOUT (-5)     /* device status: a bounded wait gave up */
+#define MOE_ERR_TIMEOUT (-5)     /* a bounded wait inside a kernel gave up */
 
 /* ---- element types ------------------------------------------------------ */
 #define MOE_BF16 0           /* bfloat16 */
@@ -118,7 +121,8 @@ typedef struct MoeSizes {
     int64_t partial_slots;       /* P = min(R, N): partial rows per token */
     int64_t partial_bytes;       /* [N*T][P][H] of y_dtype (moe_combine_partials) */
     int64_t slot_rank_bytes;     /* i32 [N*T][P] */
-    int64_t fused_workspace_bytes; /* workspace of moe_dispatch_fused */
+    int64_t fused_workspace_bytes; /* workspace of moe_dispatch_fused (zero-fill once before first use;
+                                      0 when no fused form that uses one takes the batch) */
 } MoeSizes;
 
 /* Fill *out with the buffer sizes for dims (host only, no CUDA call).
@@ -200,12 +204,15 @@ int moe_dispatch_pack(const MoeDims *dims, const void *x, const float *x_scales,
                       int32_t *packed_src, void *stream);
 
 /* Decode-fused dispatch: moe_route_topk, moe_dispatch_count and
- * moe_dispatch_pack in one launch, with the same arguments and identical
+ * moe_dispatch_pack in one call, with the same arguments and identical
  * outputs.  Source: "Hosting Qwen on Blackwell", section "Expert parallel"
  * (for decode the whole dispatch kernel is fused into one).
  *   workspace  device scratch of MoeSizes.fused_workspace_bytes bytes,
- *              16-byte aligned, owned by the caller; calls that may run at
- *              the same time need separate workspaces.
+ *              16-byte aligned, owned by the caller, ZERO-FILLED BEFORE ITS
+ *              FIRST USE (cudaMemset once after allocating it).  Every call
+ *              leaves it ready for the next one, so it is set up once and
+ *              reused; calls that may run at the same time need separate
+ *              workspaces.
  * Decode batches only, in one of two forms (else MOE_ERR_UNSUPPORTED before
  * anything is enqueued: use the three calls):
  *   - N*T <= 512, E <= 256 and at most 1 MB of rows read and written per 32
@@ -213,19 +220,17 @@ int moe_dispatch_pack(const MoeDims *dims, const void *x, const float *x_scales,
  *     cluster whose blocks own 32 tokens each and exchange only per-expert
  *     counts through distributed shared memory (no grid barrier; the
  *     workspace is not touched);
- *   - otherwise N*T <= 4096, R <= 16, E <= 512, any T: route and count in
- *     one cooperative launch (all its blocks resident at once, two per SM,
- *     each routing and counting its own run of at most 32 tokens; the
- *     per-block histograms meet in the workspace, where the block that
- *     finishes last scans them and releases the others), then the pack
- *     kernel, which starts as the first one ends.  The wait for the release
- *     is bounded; one that gives up leaves MOE_ERR_TIMEOUT in *status.  The
- *     call clears the workspace's first 512 bytes before the launch.
- * On GB300 the fused call beats the three separate calls only on small
+ *   - otherwise N*T <= 4096 and E <= 512, any T and R: two kernels.  The
+ *     first routes the tokens in blocks of at most 32 (never across a
+ *     source rank), records each pair's rank among its block's pairs of the
+ *     same expert and publishes the block's per-expert counts to the
+ *     workspace; the block that finishes last scans them into per-block
+ *     prefixes and the count outputs.  No block waits for another.  The
+ *     second is the pack kernel, which derives each pair's row from those
+ *     and writes pos as it packs.
+ * On GB300 the single-cluster form beats the three separate calls on small
  * batches with small rows (256 tokens with R = 2 and 2 KB rows: 12.8 vs
- * 15.7 us).  On the 4096-token DeepSeek-V3- and Kimi-K2-shaped decode
- * batches the separate calls, which already overlap their launches, are
- * faster (DeepSeek-V3: about 95 vs 87 us). 
+ * 15.7 us).
  * An empty batch (N*T == 0) is always accepted: like moe_dispatch_count it
  * writes zero counts and offsets and MOE_OK (the workspace is not touched). */
 int moe_dispatch_fused(const MoeDims *dims, const float *logits, const float *bias, int score_fn,
@@ -242,19 +247,20 @@ int moe_dispatch_fused(const MoeDims *dims, const float *logits, const float *bi
  * its hot path, where it would synchronise the device and could fail under
  * memory pressure).  The pages have no counterpart: this is a deployment
  * convenience of this library.
- *   Scratch: a fixed array of 192 KiB in the library's device memory,
+ *   Scratch: a fixed array of 256 KiB in the library's device memory,
  *   reserved on every GPU that loads the library until the process exits
- *   (enough for every batch moe_dispatch_fused accepts: E <= 512 needs at
- *   most 186,896 bytes; larger needs are rejected with MOE_ERR_UNSUPPORTED).
+ *   (enough for every batch moe_dispatch_fused accepts: N*T <= 4096 and
+ *   E <= 512 need at most 216,064 bytes; larger needs are rejected with
+ *   MOE_ERR_UNSUPPORTED).  It starts zero-filled and every call leaves it
+ *   ready for the next.
  *   The first call on a device looks up the array's device address (with
  *   that device current); make that first call before any stream capture.
  *   The address is cached per device and CUDA context: after
  *   cudaDeviceReset the next call looks it up again, so after a reset, too,
  *   make one call before capturing.  The call itself allocates nothing.
- *   Every call shares the one array, which keeps the last call's contents;
- *   each call clears the words that must start at zero.  Calls that overlap
- *   on the GPU (other streams, other host threads) race on the array and
- *   must be ordered by the caller.
+ *   Every call shares the one array, which keeps the last call's contents.
+ *   Calls that overlap on the GPU (other streams, other host threads) race
+ *   on the array and must be ordered by the caller.
  * Other arguments, outputs and limits as moe_dispatch_fused. */
 int moe_dispatch_fused_static(const MoeDims *dims, const float *logits, const float *bias, int score_fn,
                               int renormalize, const void *x, const float *x_scales, int32_t *topk_idx,
@@ -341,10 +347,9 @@ int moe_combine_reduce_partials(const MoeDims *dims, const void *partial, const 
  * MOE_ERR_CUDA if the wait or the copy failed. */
 int moe_read_status(const int32_t *status, void *stream);
 
-/* Self-test of the library's bounded waits (the pages have no counterpart:
- * this is a diagnostic of this implementation).  Enqueues one thread that
- * waits, with the same bounded poll the decode-fused kernel uses for its
- * release (a sleep of 32 ns doubling to 128 ns between polls), for
+/* Self-test of a bounded wait (the pages have no counterpart: this is a
+ * diagnostic of this implementation).  Enqueues one thread that waits, with
+ * a bounded poll (a sleep of 32 ns doubling to 128 ns between polls), for
  * status[1] to become nonzero, at most `polls` times (1 <= polls <= 2^20,
  * well under a second at the upper end).  status[0] then becomes MOE_OK if
  * the word changed and MOE_ERR_TIMEOUT if the wait gave up.  Nothing in the

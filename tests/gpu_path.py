@@ -113,7 +113,7 @@ class GpuRun:
         fill_sentinels(b.packed_x, b.packed_scales, b.packed_src)
         if fused:
             assert topk_idx_override is None
-            ws = torch.empty(b.sizes["fused_workspace_bytes"], dtype=torch.uint8, device=dev)
+            ws = torch.zeros(b.sizes["fused_workspace_bytes"], dtype=torch.uint8, device=dev)
             moe.dispatch_fused(self.dims, self.d.logits, self.d.bias, w.score_fn, w.renormalize,
                                self.d.x, self.d.x_scales, b.topk_idx, b.topk_w, b.expert_counts,
                                b.expert_offsets, b.rank_counts, b.rank_offsets, b.send_counts,

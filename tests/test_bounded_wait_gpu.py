@@ -1,9 +1,8 @@
 """Failure detection without a GPU fault: a bounded wait of the library that
 is never satisfied gives up, reports MOE_ERR_TIMEOUT through a status word
 the host reads, and leaves the context usable.  The wait polls a device word
-that nothing writes (moe_selftest_bounded_wait, the same bounded poll as the
-decode-fused kernel's release wait) with a small limit, so it ends within a
-few milliseconds."""
+that nothing writes (moe_selftest_bounded_wait) with a small limit, so it
+ends within a few milliseconds."""
 import pytest
 import torch
 

@@ -7,8 +7,8 @@ reset set them again.  This runs in a child process that uses the C ABI and
 the CUDA runtime through ctypes only (PyTorch's allocator does not survive a
 device reset): the count of a 5120-token batch with E = 512 (1024-thread
 blocks, about 96 KB of shared memory) and the fused dispatch of a 256-token
-batch (single cluster) and a 1024-token batch (cooperative route-count
-kernel), before and after a reset, with identical outputs."""
+batch (single cluster) and a 1024-token batch (route kernel that counts,
+then the pack kernel), before and after a reset, with identical outputs."""
 import os
 import subprocess
 import sys
@@ -68,7 +68,7 @@ def count_round():
 
 def fused_round(T):
     # T = 64: 256 tokens, the single-cluster kernel; T = 256: 1024 tokens,
-    # the cooperative route-count kernel and the pack kernel
+    # the route kernel that counts and the pack kernel
     N, E, R, H = 4, 32, 4, 64
     NT = N * T
     logits = rng.standard_normal((NT, E)).astype(np.float32)
@@ -79,6 +79,7 @@ def fused_round(T):
                  ro=4 * (N + 1), sc=4 * N * N, pos=4 * NT * R, st=4, px=2 * H * N * cap, ps=4 * N * cap, ws=1 << 20)
     st = np.empty(1, np.int32)
     b = {k: dmalloc(n) for k, n in sizes.items()}
+    assert rt.cudaMemset(b["ws"], 0, ctypes.c_size_t(sizes["ws"])) == 0  # zero-filled before first use
     h2d(b["lg"], logits)
     h2d(b["x"], x)
     rc = lib.moe_dispatch_fused(ctypes.byref(d), b["lg"], None, 0, 1, b["x"], None, b["ti"], b["tw"], b["ec"],
@@ -97,13 +98,13 @@ def fused_round(T):
 lib.moe_last_error.restype = ctypes.c_char_p
 rng = np.random.default_rng(5)
 a_pos, a_ec = count_round()
-a_small, a_coop = fused_round(64), fused_round(256)
+a_small, a_two = fused_round(64), fused_round(256)
 assert rt.cudaDeviceReset() == 0
 rng = np.random.default_rng(5)
 b_pos, b_ec = count_round()
-b_small, b_coop = fused_round(64), fused_round(256)
+b_small, b_two = fused_round(64), fused_round(256)
 assert (a_pos == b_pos).all() and (a_ec == b_ec).all()
-assert (a_small == b_small).all() and (a_coop == b_coop).all()
+assert (a_small == b_small).all() and (a_two == b_two).all()
 assert int(a_ec.sum()) == 4 * 1280 * 8
 print("RESET_OK")
 '''

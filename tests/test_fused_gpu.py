@@ -1,6 +1,7 @@
-"""Parity of the decode-fused dispatch (route + count + pack in one launch:
-one thread-block cluster for small batches, else one cooperative launch)
-with the oracle; same bar as the separate calls: indices, counts, positions
+"""Parity of the decode-fused dispatch (route + count + pack in one call:
+one thread-block cluster for small batches, else a route kernel that also
+counts, whose last block scans the counts, followed by a pack kernel that
+derives the rows itself) with the oracle; same bar as the separate calls: indices, counts, positions
 and packed rows bit-exact (and nothing written outside the occupied rows),
 weights within 2e-6, combine within the combine tolerance."""
 import numpy as np
@@ -47,30 +48,37 @@ CASES = {
     # E = 256, R = 8 (rows of 512 bytes: 147 KB read and written per block)
     "small_max": W.Workload("small_max", N=16, T=32, E=256, R=8, H=256, score_fn=W.SIGMOID,
                             renormalize=True, bias="normal", seed=66),
-    # odd E: the single-cluster path (64 tokens) and the cooperative kernel (960 tokens)
+    # odd E: the single-cluster path (64 tokens) and the two-kernel form (960 tokens)
     "odd_e_small": W.Workload("odd_e_small", N=1, T=64, E=7, R=3, H=64, seed=69),
-    "odd_e_coop": W.Workload("odd_e_coop", N=3, T=320, E=9, R=3, H=64, seed=70),
-    # 256 tokens with 14 KB rows: too much row traffic for the cluster path, so
-    # the cooperative kernel runs with one token per block
-    "coop_one_token_blocks": W.Workload("coop_one_token_blocks", N=2, T=128, E=16, R=4, H=7168,
-                                        score_fn=W.SIGMOID, renormalize=True, bias="normal",
-                                        expert_op=W.EXPERT_SCALE, seed=71),
-    # cooperative kernel, T not a multiple of 32 (blocks straddle source ranks)
-    "coop_t100": W.Workload("coop_t100", N=8, T=100, E=64, R=6, H=256, renormalize=True,
-                            bias="normal", seed=74),
-    # cooperative kernel, R = 16 (512 pairs in a block of 32 tokens at most)
-    "coop_r16": W.Workload("coop_r16", N=4, T=160, E=64, R=16, H=128, score_fn=W.SIGMOID, seed=75),
-    # cooperative kernel, one token per rank and 512 ranks: blocks of one or
-    # two tokens, each from its own source rank
-    "coop_t1_n512": W.Workload("coop_t1_n512", N=512, T=1, E=512, R=4, H=64, bias="normal",
-                               seed=76),
-    # cooperative kernel at its largest batch with the widest expert table
-    # (4096 tokens, E = 512: 16 experts per lane)
-    "coop_4096_e512": W.Workload("coop_4096_e512", N=16, T=256, E=512, R=8, H=256,
-                                 score_fn=W.SIGMOID, renormalize=True, bias="normal", seed=77),
-    # cooperative kernel, capacity overflow
-    "coop_capacity": W.Workload("coop_capacity", N=8, T=96, E=32, R=4, H=128, cap_rows=300,
-                                seed=78),
+    "odd_e_two_kernel": W.Workload("odd_e_two_kernel", N=3, T=320, E=9, R=3, H=64, seed=70),
+    # 256 tokens with 14 KB rows: too much row traffic for the cluster path
+    "wide_rows_256": W.Workload("wide_rows_256", N=2, T=128, E=16, R=4, H=7168,
+                                score_fn=W.SIGMOID, renormalize=True, bias="normal",
+                                expert_op=W.EXPERT_SCALE, seed=71),
+    # T not a multiple of 32: four blocks per source rank, the last with 4 tokens
+    "t100": W.Workload("t100", N=8, T=100, E=64, R=6, H=256, renormalize=True,
+                       bias="normal", seed=74),
+    # R = 16 (512 pairs in a block of 32 tokens)
+    "r16": W.Workload("r16", N=4, T=160, E=64, R=16, H=128, score_fn=W.SIGMOID, seed=75),
+    # R = 32: 1024 pairs, one per thread of a route block
+    "r32": W.Workload("r32", N=4, T=192, E=64, R=32, H=64, renormalize=True, seed=79),
+    # one token per rank and 512 ranks: blocks of 32 whole source ranks
+    "t1_n512": W.Workload("t1_n512", N=512, T=1, E=512, R=4, H=64, bias="normal", seed=76),
+    # T = 5: six whole source ranks per block, the last block with two
+    "t5_n200": W.Workload("t5_n200", N=200, T=5, E=400, R=4, H=64, renormalize=True, seed=80),
+    # T = 17: one whole source rank per block, 17 tokens each
+    "t17": W.Workload("t17", N=48, T=17, E=96, R=5, H=64, score_fn=W.SIGMOID, seed=81),
+    # T = 33: two blocks per source rank, the second with one token; the
+    # largest workspace of the fused form (248 route blocks, E = 496)
+    "t33_n124_e496": W.Workload("t33_n124_e496", N=124, T=33, E=496, R=8, H=64, renormalize=True,
+                                seed=82),
+    # the largest batch with the widest expert table (4096 tokens, E = 512:
+    # 16 experts per lane)
+    "n4096_e512": W.Workload("n4096_e512", N=16, T=256, E=512, R=8, H=256,
+                             score_fn=W.SIGMOID, renormalize=True, bias="normal", seed=77),
+    # capacity overflow
+    "capacity_two_kernel": W.Workload("capacity_two_kernel", N=8, T=96, E=32, R=4, H=128,
+                                      cap_rows=300, seed=78),
     # shapes only the single-cluster path takes: one token per rank (T % 32
     # != 0) and R > 8
     "decode_t1": W.Workload("decode_t1", N=64, T=1, E=128, R=8, H=256, score_fn=W.SIGMOID,
@@ -78,7 +86,7 @@ CASES = {
     "r12_t24": W.Workload("r12_t24", N=8, T=24, E=64, R=12, H=128, renormalize=True, seed=73),
     # a cluster of one block: one rank, 32 tokens
     "one_block": W.Workload("one_block", N=1, T=32, E=8, R=2, H=64, bias="normal", seed=68),
-    # past the cluster path's per-block row traffic (1.2 MB): cooperative kernel
+    # past the cluster path's per-block row traffic (1.2 MB): two-kernel form
     "past_small": W.Workload("past_small", N=16, T=32, E=256, R=8, H=2048, score_fn=W.SIGMOID,
                              renormalize=True, bias="normal", seed=67),
 }
@@ -89,14 +97,16 @@ def test_fused_cases(name):
     w = CASES[name]
     inp = W.make_inputs(w, tie_every=3 if name == "ties_sigmoid" else 0)
     gr, _, _ = _compare(w, inp, fused=True)
-    assert gr.status == (oracle.ERR_CAPACITY if name in ("capacity", "coop_capacity") else oracle.OK)
+    assert gr.status == (oracle.ERR_CAPACITY if name in ("capacity", "capacity_two_kernel") else oracle.OK)
 
 
-# dsv3_decode, kimi_k2_decode, past_small and the coop_ cases take the
-# cooperative kernel; tiny and small_max the single thread-block cluster (up
-# to 512 tokens, E <= 256, at most 1 MB of rows read and written per 32 tokens)
+# dsv3_decode, kimi_k2_decode, past_small, t100, r16, r32, t1_n512, t5_n200
+# and t33_n124_e496 take the two-kernel form; tiny, small_max, decode_t1 and
+# r12_t24 the single thread-block cluster (up to 512 tokens, E <= 256, at most
+# 1 MB of rows read and written per 32 tokens)
 @pytest.mark.parametrize("name", ["dsv3_decode", "kimi_k2_decode", "past_small", "tiny", "small_max",
-                                  "decode_t1", "r12_t24", "coop_t100", "coop_r16", "coop_t1_n512"])
+                                  "decode_t1", "r12_t24", "t100", "r16", "r32", "t1_n512", "t5_n200",
+                                  "t33_n124_e496"])
 def test_fused_equals_separate_calls_bytewise(name):
     w = W.WORKLOADS.get(name) or CASES[name]
     inp = W.make_inputs(w)
@@ -111,11 +121,11 @@ def test_fused_equals_separate_calls_bytewise(name):
 
 
 @pytest.mark.parametrize("static", [False, True])
-@pytest.mark.parametrize("R", [2, 17])  # R = 17 is past both fused kernels' limits
-def test_fused_empty_batch(static, R):
+@pytest.mark.parametrize("E", [32, 1024])  # E = 1024 is past both fused forms' limits
+def test_fused_empty_batch(static, E):
     """N*T == 0 is always accepted: zero counts and offsets, MOE_OK, as the
     separate calls give."""
-    w = W.Workload("empty", N=4, T=0, E=32, R=R, H=64)
+    w = W.Workload("empty", N=4, T=0, E=E, R=17, H=64)
     dims = moe.dims_of(w)
     b = moe.Buffers(dims)
     for t in (b.expert_counts, b.expert_offsets, b.rank_counts, b.rank_offsets, b.send_counts):
@@ -129,7 +139,9 @@ def test_fused_empty_batch(static, R):
     if static:
         moe.dispatch_fused_static(*args)
     else:
-        ws = torch.empty(moe.buffer_sizes(dims)["fused_workspace_bytes"], dtype=torch.uint8,
+        # a workspace of at least one byte: the call requires a pointer even
+        # where it does not use it
+        ws = torch.zeros(max(1, moe.buffer_sizes(dims)["fused_workspace_bytes"]), dtype=torch.uint8,
                          device="cuda")
         moe.dispatch_fused(*args, ws)
     assert moe.read_status(b.status) == moe.MOE_OK
@@ -139,9 +151,9 @@ def test_fused_empty_batch(static, R):
 
 @pytest.mark.parametrize("name", ["tiny", "dsv3_decode"])
 def test_fused_dispatch_captures_into_a_cuda_graph(name):
-    """moe_dispatch_fused enqueues only stream work with fixed shapes (the
-    single-cluster kernel, or a memset, the cooperative route-count kernel
-    and the pack kernel), so it captures into a CUDA graph; a replay on new
+    """moe_dispatch_fused enqueues only kernels with fixed shapes (the
+    single-cluster kernel, or the route kernel that counts and the pack
+    kernel), so it captures into a CUDA graph; a replay on new
     inputs gives the oracle's routing, counts, positions and rows."""
     w = W.WORKLOADS[name]
     dims = moe.dims_of(w)
@@ -149,7 +161,7 @@ def test_fused_dispatch_captures_into_a_cuda_graph(name):
     inp = W.make_inputs(w, device="cuda")
     logits, x = inp.logits.clone(), inp.x.clone()
     bias = None if inp.bias is None else inp.bias.clone()
-    ws = torch.empty(b.sizes["fused_workspace_bytes"], dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(b.sizes["fused_workspace_bytes"], dtype=torch.uint8, device="cuda")
 
     def call():
         moe.dispatch_fused(dims, logits, bias, w.score_fn, w.renormalize, x, None, b.topk_idx,

@@ -1,7 +1,7 @@
 """Seeded sweeps of random shapes through the other entry points, each at the
 bar of its own tests:
 
-* decode-fused dispatch (both the single-cluster and the cooperative path)
+* decode-fused dispatch (both the single-cluster and the two-kernel form)
   against the three separate calls, byte for byte;
 * the quantising pack against the oracle (codes and scales bit-exact);
 * the expert-parallel local path of a rank and the send-side partials
@@ -48,12 +48,12 @@ def _fused_shapes(n, seed=31):
     rng = random.Random(seed)
     out = []
     for i in range(n):
-        N = rng.choice([1, 2, 3, 4, 8, 16])
+        N = rng.choice([1, 2, 3, 4, 8, 16, 32, 64, 128])
         E = N * rng.choice([1, 2, 3, 5, 8, 16, 32])
         while E > 512:
             E //= 2
         E = max(N, E // N * N)
-        R = rng.randint(1, min(E, 16))
+        R = rng.randint(1, min(E, 32))
         T = rng.randint(1, max(1, min(256, 4096 // N)))
         x_dtype, H, y_dtype, op = _rows(rng)
         score = rng.choice([W.SOFTMAX, W.SIGMOID]) | (FLAG if rng.random() < 0.25 else 0)

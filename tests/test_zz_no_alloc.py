@@ -47,7 +47,7 @@ def _dispatch(w: W.Workload, d: W.Inputs, static: bool) -> dict:
     if static:
         moe.dispatch_fused_static(*args)
     else:
-        ws = torch.empty(b.sizes["fused_workspace_bytes"], dtype=torch.uint8, device=d.logits.device)
+        ws = torch.zeros(b.sizes["fused_workspace_bytes"], dtype=torch.uint8, device=d.logits.device)
         moe.dispatch_fused(*args, ws)
     torch.cuda.synchronize()
     return {k: getattr(b, k).view(torch.uint8 if k == "packed_x" else getattr(b, k).dtype).cpu().numpy()
