@@ -9,13 +9,14 @@ route + count + pack with scratch that lives in the library itself.
 
 The GPU test calls it through the C ABI several times in a row, on batches
 of different shapes, and then checks every output of each call against
-moe_dispatch_fused given a freshly allocated (uninitialised) workspace.
+moe_dispatch_fused given a freshly allocated, zero-filled workspace.
 The calls shrink from the widest scratch use to a narrower one: 512
-experts and 16 counting blocks, then 256 experts and 16 blocks, then 96
-experts, 4 ranks and 3 blocks.  Each later call sees the scratch as the
-previous one left it, including histogram and staging words past its own
-experts, ranks and blocks, so a call that read anything it had not written
-or cleared first would show up there.  Integer outputs and packed rows must be equal
+experts and 128 route blocks, then 256 experts and 128 blocks, then 96
+experts, 4 ranks and 20 blocks.  Each later call sees the scratch as the
+previous one left it, including histogram, prefix and send-count words past
+its own experts, ranks and blocks, so a call that read anything it had not
+written first, or that left the arrival counter off zero, would show up
+there.  Integer outputs and packed rows must be equal
 byte for byte; router weights within the relative 2e-6 that the other
 parity tests allow (both calls run the same kernel, so they agree exactly
 in practice).
@@ -54,8 +55,8 @@ def _dispatch(w: W.Workload, d: W.Inputs, static: bool) -> dict:
             for k in OUTPUTS}
 
 
-# cooperative-kernel batches (more than 512 tokens, T % 32 == 0, R <= 8),
-# widest scratch use first.  Receive regions of 4096 rows per rank (the
+# batches of the two-kernel form (more than 512 tokens), widest scratch use
+# first.  Receive regions of 4096 rows per rank (the
 # largest rank receives 2774, 1945 and 1001 rows) keep the buffers compared
 # on the host small; the capacity does not change what the scratch holds.
 STATIC_SEQUENCE = (
