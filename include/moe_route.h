@@ -65,7 +65,7 @@ extern "C" {
 #define MOE_ERR_UNSUPPORTED (-2) /* valid request this build does not implement */
 #define MOE_ERR_CUDA (-3)        /* a CUDA runtime call or kernel launch failed */
 #define MOE_ERR_CAPACITY (-4)    /* device status: a rank received more than cap_rows rows */
-#define MOE_ERR_TIMEOUT (-5)     /* a bounded wait inside a kernel gave up */
+#define MOE_ERR_TIMEOUT (-5)     /* device status: a bounded wait gave up */
 
 /* ---- element types ------------------------------------------------------ */
 #define MOE_BF16 0           /* bfloat16 */
