@@ -50,6 +50,21 @@ __device__ __forceinline__ void sort_desc(uint32_t (&k)[JP], int (&sl)[JP]) {
     }
 }
 
+// Best live slot of a lane: the highest key, the lowest slot among equal
+// keys (slots are scanned in ascending order and only a strictly higher key
+// replaces the best).  s = -1 when no slot is live.
+template <int J>
+__device__ __forceinline__ void lane_best(const uint32_t (&key)[J], uint32_t live, uint32_t &h, int &s) {
+    h = 0u;
+    s = -1;
+#pragma unroll
+    for (int j = 0; j < J; ++j)
+        if (((live >> j) & 1u) && (s < 0 || key[j] > h)) {
+            h = key[j];
+            s = j;
+        }
+}
+
 // Route token g with the calling warp (all 32 lanes).  Returns, in lane
 // k < R, the expert of pair k (what it writes to topk_idx[g][k]).
 template <int J, bool kVec4>
@@ -113,56 +128,104 @@ __device__ __forceinline__ int route_token(const float *__restrict__ logits,
                 if (e0 + j < E) z[j] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z[j])));
         }
     }
-    // JP >= J slots (a power of two for the sorting network); padding
-    // slots carry key 0 and sort last
-    constexpr int JP = (J <= 1) ? 1 : (J <= 2) ? 2 : (J <= 4) ? 4 : (J <= 8) ? 8 : (J <= 16) ? 16 : 32;
     uint32_t valid = 0;
-    uint32_t key[JP];
-    int slot[JP];
+    uint32_t key[J];
 #pragma unroll
-    for (int j = 0; j < JP; ++j) {
+    for (int j = 0; j < J; ++j) {
         key[j] = 0u;
-        slot[j] = j;
-        if (j < J && e0 + j < E) {
+        if (e0 + j < E) {
             valid |= 1u << j;
             if (bias != nullptr) z[j] = __fadd_rn(z[j], __ldg(bias + e0 + j));
             key[j] = order_key(z[j]);
         }
     }
-    int left = __popc(valid);  // live keys of this lane
-    uint32_t sk[JP];
-    int ss[JP];
-#pragma unroll
-    for (int j = 0; j < JP; ++j) {
-        sk[j] = key[j];
-        ss[j] = slot[j];
-    }
-    sort_desc<JP>(sk, ss);
-
-    // R rounds of warp arg-max over the lanes' heads; the winning lane pops
-    // its head (a register shift, no rescan).
+    // R rounds of a warp max reduction (redux.sync) over one key per lane (the
+    // lane's best remaining key) and a ballot for the lowest lane holding the
+    // maximum: highest key, then lowest lane, then lowest slot.  How a lane
+    // keeps its best key depends on how many it holds:
+    //   J <= 8: it sorts its keys once (bitonic network, key descending, slot
+    //   ascending) and the winning lane shifts its sorted keys by one;
+    //   J >= 12: it keeps its best and second-best keys, the winning lane
+    //   promotes its runner-up, and only a lane that wins a third time
+    //   rescans its remaining keys (sorting 12 or more keys per lane doubled
+    //   the instructions per token on the 384-expert batch, where routing is
+    //   bound by instruction issue; with 4 or 8 keys the sort is cheaper).
     float zmax = 0.f;
     int my_e = 0;
     float my_z = 0.f;
-    for (int k = 0; k < R; ++k) {
-        const uint32_t v = (left > 0) ? sk[0] : 0u;
-        const uint32_t kmax = __reduce_max_sync(kFull, v);
-        const unsigned ball = __ballot_sync(kFull, left > 0 && v == kmax);
-        const int wl = __ffs(ball) - 1;  // some lane always has a live key (R <= E)
-        const int wj = __shfl_sync(kFull, ss[0], wl);
-        const float wz = key_value(kmax);
-        if (k == 0) zmax = wz;
-        if (lane == k) {
-            my_e = wl * J + wj;
-            my_z = wz;
-        }
-        if (lane == wl) {
+    if constexpr (J <= 8) {
+        constexpr int JP = (J <= 1) ? 1 : (J <= 2) ? 2 : (J <= 4) ? 4 : 8;
+        uint32_t sk[JP];
+        int ss[JP];
 #pragma unroll
-            for (int j = 0; j + 1 < JP; ++j) {
-                sk[j] = sk[j + 1];
-                ss[j] = ss[j + 1];
+        for (int j = 0; j < JP; ++j) {
+            sk[j] = j < J ? key[j] : 0u;  // padding slots carry key 0 and sort last
+            ss[j] = j;
+        }
+        sort_desc<JP>(sk, ss);
+        int left = __popc(valid);  // live keys of this lane
+        for (int k = 0; k < R; ++k) {
+            const uint32_t v = (left > 0) ? sk[0] : 0u;
+            const uint32_t kmax = __reduce_max_sync(kFull, v);
+            const unsigned ball = __ballot_sync(kFull, left > 0 && v == kmax);
+            const int wl = __ffs(ball) - 1;  // some lane always has a live key (R <= E)
+            const int wj = __shfl_sync(kFull, ss[0], wl);
+            const float wz = key_value(kmax);
+            if (k == 0) zmax = wz;
+            if (lane == k) {
+                my_e = wl * J + wj;
+                my_z = wz;
             }
-            --left;
+            if (lane == wl) {
+#pragma unroll
+                for (int j = 0; j + 1 < JP; ++j) {
+                    sk[j] = sk[j + 1];
+                    ss[j] = ss[j + 1];
+                }
+                --left;
+            }
+        }
+    } else {
+        uint32_t live = valid;
+        uint32_t h1 = 0u, h2 = 0u;
+        int s1 = -1, s2 = -1;
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            if ((live >> j) & 1u) {
+                if (s1 < 0 || key[j] > h1) {
+                    h2 = h1;
+                    s2 = s1;
+                    h1 = key[j];
+                    s1 = j;
+                } else if (s2 < 0 || key[j] > h2) {
+                    h2 = key[j];
+                    s2 = j;
+                }
+            }
+        }
+        bool second = true;  // (h2, s2) is the lane's runner-up (s2 = -1: none left)
+        for (int k = 0; k < R; ++k) {
+            const bool has = s1 >= 0;
+            const uint32_t kmax = __reduce_max_sync(kFull, has ? h1 : 0u);
+            const unsigned ball = __ballot_sync(kFull, has && h1 == kmax);
+            const int wl = __ffs(ball) - 1;  // some lane always has a live key (R <= E)
+            const int wj = __shfl_sync(kFull, s1, wl);
+            const float wz = key_value(kmax);
+            if (k == 0) zmax = wz;
+            if (lane == k) {
+                my_e = wl * J + wj;
+                my_z = wz;
+            }
+            if (lane == wl) {
+                live &= ~(1u << s1);
+                if (second) {
+                    h1 = h2;
+                    s1 = s2;
+                    second = false;
+                } else {
+                    lane_best<J>(key, live, h1, s1);
+                }
+            }
         }
     }
 
