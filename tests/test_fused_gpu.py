@@ -37,9 +37,14 @@ CASES = {
     # one expert per rank, f32 rows, N*T = 672 split unevenly over the blocks
     "f32_ragged": W.Workload("f32_ragged", N=7, T=96, E=14, R=2, H=72, x_dtype=W.F32,
                              y_dtype=W.F32, renormalize=True, seed=62),
-    # fp8 rows with block scales
+    # fp8 rows with block scales (512 tokens: the single-cluster path)
     "fp8": W.Workload("fp8", N=8, T=64, E=64, R=4, H=512, x_dtype=W.FP8E4M3_BLK128,
                       expert_op=W.EXPERT_DEQUANT, seed=63),
+    # fp8 rows with block scales through the two-kernel form (1536 tokens,
+    # three route blocks per source rank)
+    "fp8_two_kernel": W.Workload("fp8_two_kernel", N=16, T=96, E=128, R=8, H=1024,
+                                 x_dtype=W.FP8E4M3_BLK128, expert_op=W.EXPERT_DEQUANT,
+                                 renormalize=True, seed=83),
     # more experts per lane (E = 512)
     "e512": W.Workload("e512", N=16, T=64, E=512, R=8, H=128, renormalize=True, seed=64),
     # capacity overflow reported through the status word
@@ -100,13 +105,13 @@ def test_fused_cases(name):
     assert gr.status == (oracle.ERR_CAPACITY if name in ("capacity", "capacity_two_kernel") else oracle.OK)
 
 
-# dsv3_decode, kimi_k2_decode, past_small, t100, r16, r32, t1_n512, t5_n200
-# and t33_n124_e496 take the two-kernel form; tiny, small_max, decode_t1 and
+# dsv3_decode, kimi_k2_decode, past_small, t100, r16, r32, t1_n512, t5_n200,
+# t33_n124_e496 and fp8_two_kernel take the two-kernel form; tiny, small_max, decode_t1 and
 # r12_t24 the single thread-block cluster (up to 512 tokens, E <= 256, at most
 # 1 MB of rows read and written per 32 tokens)
 @pytest.mark.parametrize("name", ["dsv3_decode", "kimi_k2_decode", "past_small", "tiny", "small_max",
                                   "decode_t1", "r12_t24", "t100", "r16", "r32", "t1_n512", "t5_n200",
-                                  "t33_n124_e496"])
+                                  "t33_n124_e496", "fp8_two_kernel"])
 def test_fused_equals_separate_calls_bytewise(name):
     w = W.WORKLOADS.get(name) or CASES[name]
     inp = W.make_inputs(w)
@@ -114,10 +119,12 @@ def test_fused_equals_separate_calls_bytewise(name):
     b = GpuRun(w, inp)
     for k in a.host:
         np.testing.assert_array_equal(a.host[k], b.host[k], err_msg=k)
-    pa, _, sa = a.packed_rows()
-    pb, _, sb = b.packed_rows()
+    pa, sca, sa = a.packed_rows()
+    pb, scb, sb = b.packed_rows()
     np.testing.assert_array_equal(pa, pb)
     np.testing.assert_array_equal(sa, sb)
+    if sca is not None or scb is not None:  # fp8 rows: the block scales too
+        np.testing.assert_array_equal(sca, scb)
 
 
 @pytest.mark.parametrize("static", [False, True])
