@@ -199,3 +199,48 @@ def test_rank_entries_reject_ranks_outside_the_batch(lib):
         assert lib.moe_combine_rank(ctypes.byref(d), rank, ok, ok, ok, ok,
                                     None) == moe.MOE_ERR_INVALID_ARG
         assert "outside [0, 4)" in lib.moe_last_error().decode()
+
+
+def _fused_workspace_layout(N, T, E):
+    """The two-kernel fused dispatch's workspace, restated: a 256-byte header
+    (the arrival counter), one byte per expert per route block, a u16 prefix
+    per expert per chunk of 8 route blocks and, when source ranks are split
+    over blocks (T > 32), a u16 send count per block and destination rank;
+    every section padded to 256 bytes.  Route blocks hold at most 32 tokens
+    and never cross a source rank."""
+    a256 = lambda v: (v + 255) // 256 * 256
+    Ep = (E + 15) // 16 * 16
+    if T <= 32:
+        B, split = -(-N // (32 // T)), False
+    else:
+        B, split = N * -(-T // 32), True
+    return 256 + a256(B * Ep) + a256(-(-B // 8) * Ep * 2) + (a256(B * N * 2) if split else 0)
+
+
+@pytest.mark.parametrize("N,T,E", [(32, 128, 256), (64, 64, 384), (16, 256, 512), (4, 160, 96), (512, 1, 512),
+                                   (200, 5, 400), (48, 17, 96), (124, 33, 496), (8, 100, 64), (1, 32, 8)])
+def test_fused_workspace_size(lib, N, T, E):
+    s = moe.buffer_sizes(moe.make_dims(N, T, E, min(8, E), 64))
+    assert s["fused_workspace_bytes"] == _fused_workspace_layout(N, T, E)
+
+
+def test_fused_workspace_fits_the_static_scratch_and_is_zero_outside_the_fused_scope(lib):
+    # the largest workspace of any batch the two-kernel form takes (N*T <=
+    # 4096, E <= 512) is that of N = 124, T = 33, E = 496; the static array
+    # of moe_dispatch_fused_static holds 256 KiB
+    worst = 0
+    for N in (1, 2, 4, 8, 16, 31, 62, 124, 128, 256, 512):
+        for T in sorted({1, 2, 5, 16, 17, 31, 32, 33, 63, 64, 65, 100, 128, 4096 // N}):
+            if T < 1 or N * T > 4096:
+                continue
+            E = 512 // N * N
+            if E == 0:
+                continue
+            got = moe.buffer_sizes(moe.make_dims(N, T, E, min(8, E), 64))["fused_workspace_bytes"]
+            assert got == _fused_workspace_layout(N, T, E), (N, T, E)
+            worst = max(worst, got)
+    assert worst <= 256 * 1024
+    assert moe.buffer_sizes(moe.make_dims(124, 33, 496, 8, 64))["fused_workspace_bytes"] == 216064
+    # no fused form with a workspace takes these: more than 4096 tokens, E > 512
+    assert moe.buffer_sizes(moe.make_dims(4, 4096, 128, 8, 64))["fused_workspace_bytes"] == 0
+    assert moe.buffer_sizes(moe.make_dims(4, 64, 1024, 8, 64))["fused_workspace_bytes"] == 0
