@@ -81,6 +81,10 @@ CASES = {
     # 16 experts per lane)
     "n4096_e512": W.Workload("n4096_e512", N=16, T=256, E=512, R=8, H=256,
                              score_fn=W.SIGMOID, renormalize=True, bias="normal", seed=77),
+    # a single route block, which is also the one that scans (32 tokens of
+    # one rank with 14 KB rows: past the cluster path's row traffic)
+    "one_route_block": W.Workload("one_route_block", N=1, T=32, E=16, R=4, H=7168, score_fn=W.SIGMOID,
+                                  renormalize=True, bias="normal", seed=84),
     # capacity overflow
     "capacity_two_kernel": W.Workload("capacity_two_kernel", N=8, T=96, E=32, R=4, H=128,
                                       cap_rows=300, seed=78),
@@ -106,12 +110,12 @@ def test_fused_cases(name):
 
 
 # dsv3_decode, kimi_k2_decode, past_small, t100, r16, r32, t1_n512, t5_n200,
-# t33_n124_e496 and fp8_two_kernel take the two-kernel form; tiny, small_max, decode_t1 and
+# t33_n124_e496, fp8_two_kernel and one_route_block take the two-kernel form; tiny, small_max, decode_t1 and
 # r12_t24 the single thread-block cluster (up to 512 tokens, E <= 256, at most
 # 1 MB of rows read and written per 32 tokens)
 @pytest.mark.parametrize("name", ["dsv3_decode", "kimi_k2_decode", "past_small", "tiny", "small_max",
                                   "decode_t1", "r12_t24", "t100", "r16", "r32", "t1_n512", "t5_n200",
-                                  "t33_n124_e496", "fp8_two_kernel"])
+                                  "t33_n124_e496", "fp8_two_kernel", "one_route_block"])
 def test_fused_equals_separate_calls_bytewise(name):
     w = W.WORKLOADS.get(name) or CASES[name]
     inp = W.make_inputs(w)
