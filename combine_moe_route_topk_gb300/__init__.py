@@ -229,7 +229,8 @@ def dispatch_fused(dims: MoeDims, logits, bias, score_fn, renormalize, x, x_scal
         _ptr(packed_x, s["packed_x_bytes"], "packed_x", _TORCH_DTYPE[dims.x_dtype]),
         _ptr(packed_scales, s["packed_scales_bytes"], "packed_scales", f32, optional=not fp8),
         _ptr(packed_src, s["packed_src_bytes"], "packed_src", i32),
-        _ptr(workspace, s["fused_workspace_bytes"], "workspace"), _stream(stream)))
+        _ptr(workspace, s["fused_workspace_bytes"], "workspace", optional=dims.N * dims.T == 0),
+        _stream(stream)))
 
 
 def dispatch_fused_static(dims: MoeDims, logits, bias, score_fn, renormalize, x, x_scales,

@@ -407,13 +407,14 @@ int moe_dispatch_fused(const MoeDims *dims, const float *logits, const float *bi
     if (why[0] != '\0')
         return set_error(MOE_ERR_UNSUPPORTED, "moe_dispatch_fused: %s; use the separate calls", why);
     const bool fp8 = dims->x_dtype == MOE_FP8E4M3_BLK128;
+    // an empty batch touches no workspace (its size is 0 there): NULL is fine
     if (!expert_counts || !expert_offsets || !rank_counts || !rank_offsets || !send_counts || !status ||
-        !workspace)
+        (!workspace && v.NT > 0))
         return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_fused: a required pointer is NULL");
     if (v.NT > 0 && (!logits || !x || !topk_idx || !topk_w || !pos || !packed_x || !packed_src ||
                      (fp8 && (!x_scales || !packed_scales))))
         return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_fused: a required pointer is NULL");
-    if ((x && !aligned(x, 16)) || (packed_x && !aligned(packed_x, 16)) || !aligned(workspace, 16))
+    if ((x && !aligned(x, 16)) || (packed_x && !aligned(packed_x, 16)) || (workspace && !aligned(workspace, 16)))
         return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_fused: x, packed_x and workspace must be 16-byte aligned");
     const void *ptrs4[] = {logits, bias, topk_idx, topk_w, expert_counts, expert_offsets, rank_counts,
                            rank_offsets, send_counts, pos, status, packed_src, x_scales, packed_scales};

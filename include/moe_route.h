@@ -232,7 +232,8 @@ int moe_dispatch_pack(const MoeDims *dims, const void *x, const float *x_scales,
  * batches with small rows (256 tokens with R = 2 and 2 KB rows: 12.8 vs
  * 15.7 us).
  * An empty batch (N*T == 0) is always accepted: like moe_dispatch_count it
- * writes zero counts and offsets and MOE_OK (the workspace is not touched). */
+ * writes zero counts and offsets and MOE_OK (the workspace is not touched
+ * and may be NULL). */
 int moe_dispatch_fused(const MoeDims *dims, const float *logits, const float *bias, int score_fn,
                        int renormalize, const void *x, const float *x_scales, int32_t *topk_idx,
                        float *topk_w, int32_t *expert_counts, int32_t *expert_offsets,

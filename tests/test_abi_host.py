@@ -144,6 +144,23 @@ def test_fused_dispatch_accepts_empty_batches_of_any_shape(lib):
     assert "use the separate calls" not in lib.moe_last_error().decode()
 
 
+def test_fused_dispatch_takes_a_null_workspace_only_for_an_empty_batch(lib):
+    P = ctypes.c_void_p
+    ok = P(0x10000)
+
+    def call(d):
+        # logits, bias, score_fn, renormalize, x, x_scales, then topk_idx ..
+        # packed_x (10 pointers), packed_scales (NULL: bf16 rows), packed_src,
+        # a NULL workspace and the default stream
+        ptrs = [ok] * 10 + [None, ok]
+        return lib.moe_dispatch_fused(ctypes.byref(d), ok, None, 0, 0, ok, None, *ptrs, None, None)
+
+    assert call(moe.make_dims(N=4, T=64, E=64, R=8, H=128)) == moe.MOE_ERR_INVALID_ARG
+    assert "NULL" in lib.moe_last_error().decode()
+    rc = call(moe.make_dims(N=4, T=0, E=64, R=8, H=128))
+    assert rc != moe.MOE_ERR_INVALID_ARG  # no GPU here: at most a CUDA-level failure
+
+
 def test_rows_wider_than_2_24_elements_are_unsupported(lib):
     d = moe.make_dims(2, 8, 4, 2, (1 << 24) + 8)
     s = moe.MoeSizes()
