@@ -224,13 +224,14 @@ int moe_dispatch_pack(const MoeDims *dims, const void *x, const float *x_scales,
  *     first routes the tokens in blocks of at most 32 (never across a
  *     source rank), records each pair's rank among its block's pairs of the
  *     same expert and publishes the block's per-expert counts to the
- *     workspace; the block that finishes last scans them into per-block
- *     prefixes and the count outputs.  No block waits for another.  The
- *     second is the pack kernel, which derives each pair's row from those
- *     and writes pos as it packs.
- * On GB300 the single-cluster form beats the three separate calls on small
- * batches with small rows (256 tokens with R = 2 and 2 KB rows: 12.8 vs
- * 15.7 us).
+ *     workspace; the block that finishes last scans them into prefixes per
+ *     chunk of 8 blocks and the count outputs.  No block waits for
+ *     another.  The second is the pack kernel, which derives each pair's
+ *     row from those and writes pos as it packs.
+ * On GB300 both forms beat the three separate calls: 256 tokens with R = 2
+ * and 2 KB rows 12.5 vs 15.5 us; the DeepSeek-V3-shaped decode batch (4096
+ * tokens, 14 KB rows) 85.0 vs 85.9 us; the Kimi-K2-shaped one 87.1 vs
+ * 88.9 us.
  * An empty batch (N*T == 0) is always accepted: like moe_dispatch_count it
  * writes zero counts and offsets and MOE_OK (the workspace is not touched
  * and may be NULL). */
