@@ -24,7 +24,7 @@
 //   pack     the block copies its own tokens' rows to their positions.
 // Counts, offsets and send counts are integer sums, so every output equals
 // that of the separate route, count and pack kernels bit for bit.
-// Used for N*T <= 512 tokens (16 blocks of 32), E <= 256 and at most 1 MB of
+// Used for N*T <= 512 tokens (16 blocks of 32), E <= 256 and at most 256 KB of
 // rows read and written per block (more would be copied by too few SMs).
 #include <cooperative_groups.h>
 
@@ -44,11 +44,12 @@ constexpr int kSMaxBlocks = 16;  // non-portable cluster size limit
 constexpr int kSPackU = 4;       // row vectors per thread in flight while packing
 constexpr int kSMaxE = 256;  // 8 experts per lane: the route body fits 64 registers
 // Rows read and written per block (32 tokens x (1 + R) rows).  The pack
-// runs on at most 16 SMs; up to about this much per block it still beats
-// the cooperative kernel (measured on GB300, cluster vs cooperative: 300 KB
-// per block 21 vs 35 us, 880 KB 27 vs 34 us, 1.2 MB 33 vs 32 us, 4 MB 74 vs
-// 40 us).  The three separate calls beat both beyond about 200 KB per block.
-constexpr int64_t kSMaxBlockPackBytes = 1 << 20;
+// runs on at most 16 SMs; up to about this much per block it beats the
+// two-kernel form of dispatch_fused.cu, which packs on every SM (measured
+// on GB300, 512-token batches, cluster vs two kernels: 48-160 KB per block
+// 12.3-18.4 vs 14.4-20.5 us, 190-320 KB about equal, 384-640 KB 16.4-24.6
+// vs 14.3-20.5 us).
+constexpr int64_t kSMaxBlockPackBytes = 256 << 10;
 
 struct SmallParams {
     const float *logits;

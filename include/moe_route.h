@@ -215,8 +215,8 @@ int moe_dispatch_pack(const MoeDims *dims, const void *x, const float *x_scales,
  *              workspaces.
  * Decode batches only, in one of two forms (else MOE_ERR_UNSUPPORTED before
  * anything is enqueued: use the three calls):
- *   - N*T <= 512, E <= 256 and at most 1 MB of rows read and written per 32
- *     tokens (32 * (1 + R) * row bytes), any T and R: one thread-block
+ *   - N*T <= 512, E <= 256 and at most 256 KB of rows read and written per
+ *     32 tokens (32 * (1 + R) * row bytes), any T and R: one thread-block
  *     cluster whose blocks own 32 tokens each and exchange only per-expert
  *     counts through distributed shared memory (no grid barrier; the
  *     workspace is not touched);

@@ -95,7 +95,7 @@ CASES = {
     "r12_t24": W.Workload("r12_t24", N=8, T=24, E=64, R=12, H=128, renormalize=True, seed=73),
     # a cluster of one block: one rank, 32 tokens
     "one_block": W.Workload("one_block", N=1, T=32, E=8, R=2, H=64, bias="normal", seed=68),
-    # past the cluster path's per-block row traffic (1.2 MB): two-kernel form
+    # past the cluster path's per-block row traffic (1.2 MB of 256 KB): two-kernel form
     "past_small": W.Workload("past_small", N=16, T=32, E=256, R=8, H=2048, score_fn=W.SIGMOID,
                              renormalize=True, bias="normal", seed=67),
 }
@@ -112,7 +112,7 @@ def test_fused_cases(name):
 # dsv3_decode, kimi_k2_decode, past_small, t100, r16, r32, t1_n512, t5_n200,
 # t33_n124_e496, fp8_two_kernel and one_route_block take the two-kernel form; tiny, small_max, decode_t1 and
 # r12_t24 the single thread-block cluster (up to 512 tokens, E <= 256, at most
-# 1 MB of rows read and written per 32 tokens)
+# 256 KB of rows read and written per 32 tokens)
 @pytest.mark.parametrize("name", ["dsv3_decode", "kimi_k2_decode", "past_small", "tiny", "small_max",
                                   "decode_t1", "r12_t24", "t100", "r16", "r32", "t1_n512", "t5_n200",
                                   "t33_n124_e496", "fp8_two_kernel", "one_route_block"])

@@ -77,9 +77,13 @@ def _small_fused_shapes(n, seed=33):
         R = rng.randint(1, min(E, 32))
         T = rng.randint(1, max(1, 512 // N))
         x_dtype, H, y_dtype, op = _rows(rng)
-        H = min(H, 256)  # keep the rows within the cluster path's traffic limit
         if x_dtype == W.FP8E4M3_BLK128:
             H = 128
+        else:
+            # keep the rows within the cluster path's traffic limit: 32 tokens
+            # x (1 + R) rows of at most 256 KB per block
+            elem = 4 if x_dtype == W.F32 else 2
+            H = max(8, min(H, 256, (256 << 10) // (32 * (R + 1) * elem) // 8 * 8))
         out.append(W.Workload(f"small{i}", N=N, T=T, E=E, R=R, H=H, x_dtype=x_dtype, y_dtype=y_dtype,
                               expert_op=op, score_fn=rng.choice([W.SOFTMAX, W.SIGMOID]),
                               renormalize=rng.random() < 0.5, bias=rng.choice(["none", "normal"]),
