@@ -206,3 +206,27 @@ def test_fused_dispatch_captures_into_a_cuda_graph(name):
     crow = ref["rank_offsets"][pos // ref["cap"]] + pos % ref["cap"]
     got = oracle.x_as_bytes(b.packed_x[torch.from_numpy(pos).long().cuda()].cpu())
     np.testing.assert_array_equal(got, ref["packed_x"][crow])
+
+
+@pytest.mark.parametrize("name", ["dsv3_decode", "t33_n124_e496", "t5_n200"])
+def test_fused_call_leaves_the_workspace_ready_for_the_next(name):
+    """The two-kernel form requires a workspace whose arrival counter (its
+    first word) is zero; every call must leave it so.  A second call on the
+    same workspace then gives the same outputs as the first."""
+    w = W.WORKLOADS.get(name) or CASES[name]
+    inp = W.make_inputs(w)
+    dims = moe.dims_of(w)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    d = W.Inputs(*(t.to(dev) if t is not None else None for t in (inp.logits, inp.bias, inp.x, inp.x_scales)))
+    b = moe.Buffers(dims, device=dev)
+    ws = torch.zeros(b.sizes["fused_workspace_bytes"], dtype=torch.uint8, device=dev)
+    outs = []
+    for _ in range(2):
+        moe.dispatch_fused(dims, d.logits, d.bias, w.score_fn, w.renormalize, d.x, d.x_scales, b.topk_idx,
+                           b.topk_w, b.expert_counts, b.expert_offsets, b.rank_counts, b.rank_offsets,
+                           b.send_counts, b.pos, b.status, b.packed_x, b.packed_scales, b.packed_src, ws)
+        torch.cuda.synchronize()
+        assert int(ws[:4].view(torch.int32)[0]) == 0
+        outs.append({k: getattr(b, k).clone() for k in ("topk_idx", "expert_offsets", "send_counts", "pos")})
+    for k in outs[0]:
+        assert torch.equal(outs[0][k], outs[1][k]), k
