@@ -870,13 +870,33 @@ def variants_of(args, run, nb, host_lead, per_timed):
         with nvtx_range("pack_quant"):
             qm = run.timed_repeat(qpack, nb, host_lead)
         cm = run.timed_repeat(chain, nb, host_lead)
+        # the same fp8 dispatch as one call (decode batches only)
+        fused_fp8 = None
+        try:
+            ws = torch.zeros(max(16, moe.buffer_sizes(dims)["fused_workspace_bytes"]), dtype=torch.uint8,
+                             device=dev)
+
+            def fused_q():
+                moe.dispatch_fused_quant(dims, inp.logits, inp.bias, w.score_fn, w.renormalize, inp.x,
+                                         b.topk_idx, b.topk_w, b.expert_counts, b.expert_offsets,
+                                         b.rank_counts, b.rank_offsets, b.send_counts, b.pos, b.status,
+                                         pq, ps, b.packed_src, ws, stream)
+            with nvtx_range("fused_quant"):
+                fused_fp8 = run.timed_repeat(fused_q, nb, host_lead)
+            if moe.read_status(b.status, stream) != moe.MOE_OK:
+                raise RuntimeError("fused fp8 dispatch status")
+        except moe.MoeError:
+            fused_fp8 = None
         qbytes = w.NT * (2 * w.H + w.R * (w.H + 4 * (w.H // 128))) + w.NT * w.R * 8
         quant = {"ms": qm, "alg_bytes": qbytes, "alg_gbs": qbytes / (qm / 1e3) / 1e9,
                  "frac": qbytes / (qm / 1e3) / 1e9 / measured_peaks()[0],
                  "fp8_dispatch_ms": cm,
+                 "fused_fp8_dispatch_ms": fused_fp8,
                  "vs_bf16_dispatch_ms": per_timed["dispatch (route+count+pack)"],
                  "note": "moe_dispatch_pack_quant on the same routing, timed alone; "
-                         "fp8_dispatch_ms: route + count + quantising pack back to back"}
+                         "fp8_dispatch_ms: route + count + quantising pack back to back; "
+                         "fused_fp8_dispatch_ms: moe_dispatch_fused_quant (the same outputs in one "
+                         "call; null where the batch is not a decode batch)"}
         del pq, ps
     out["pack_quant"] = quant
 

@@ -280,6 +280,33 @@ def dispatch_pack_quant(dims: MoeDims, x, pos, packed_q, packed_scales, packed_s
         _ptr(packed_src, s["packed_src_bytes"], "packed_src", torch.int32), _stream(stream)))
 
 
+def dispatch_fused_quant(dims: MoeDims, logits, bias, score_fn, renormalize, x, topk_idx, topk_w,
+                         expert_counts, expert_offsets, rank_counts, rank_offsets, send_counts, pos,
+                         status, packed_q, packed_scales, packed_src, workspace, stream=None):
+    """Route + count + fp8-quantising pack in one call (decode batches; bf16 rows
+    in, e4m3 codes + one f32 scale per 128 elements out)."""
+    s = buffer_sizes(dims)
+    q = buffer_sizes(fp8_dims(dims))
+    i32, f32 = torch.int32, torch.float32
+    _check(lib().moe_dispatch_fused_quant(
+        ctypes.byref(dims), _ptr(logits, s["logits_bytes"], "logits", f32),
+        _ptr(bias, dims.E * 4, "bias", f32, optional=True), int(score_fn), int(bool(renormalize)),
+        _ptr(x, s["x_bytes"], "x", torch.bfloat16),
+        _ptr(topk_idx, s["topk_idx_bytes"], "topk_idx", i32),
+        _ptr(topk_w, s["topk_w_bytes"], "topk_w", f32),
+        _ptr(expert_counts, s["expert_counts_bytes"], "expert_counts", i32),
+        _ptr(expert_offsets, s["expert_offsets_bytes"], "expert_offsets", i32),
+        _ptr(rank_counts, s["rank_counts_bytes"], "rank_counts", i32),
+        _ptr(rank_offsets, s["rank_offsets_bytes"], "rank_offsets", i32),
+        _ptr(send_counts, s["send_counts_bytes"], "send_counts", i32),
+        _ptr(pos, s["pos_bytes"], "pos", i32), _ptr(status, 4, "status", i32),
+        _ptr(packed_q, q["packed_x_bytes"], "packed_q", torch.uint8),
+        _ptr(packed_scales, q["packed_scales_bytes"], "packed_scales", f32),
+        _ptr(packed_src, s["packed_src_bytes"], "packed_src", i32),
+        _ptr(workspace, s["fused_workspace_bytes"], "workspace", optional=dims.N * dims.T == 0),
+        _stream(stream)))
+
+
 def combine(dims: MoeDims, y, pos, topk_w, out, stream=None):
     s = buffer_sizes(dims)
     yt = _TORCH_DTYPE[dims.y_dtype]

@@ -433,6 +433,46 @@ int moe_dispatch_fused(const MoeDims *dims, const float *logits, const float *bi
     return cuda_result(e, "moe_dispatch_fused");
 }
 
+int moe_dispatch_fused_quant(const MoeDims *dims, const float *logits, const float *bias, int score_fn,
+                             int renormalize, const void *x, int32_t *topk_idx, float *topk_w,
+                             int32_t *expert_counts, int32_t *expert_offsets, int32_t *rank_counts,
+                             int32_t *rank_offsets, int32_t *send_counts, int32_t *pos, int32_t *status,
+                             void *packed_q, float *packed_scales, int32_t *packed_src, void *workspace,
+                             void *stream) {
+    Derived v;
+    int rc = check_dims(dims, &v, "moe_dispatch_fused_quant");
+    if (rc != MOE_OK) return rc;
+    if (!valid_score_fn(score_fn))
+        return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_fused_quant: unknown score_fn %d", score_fn);
+    if (dims->x_dtype != MOE_BF16)
+        return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_fused_quant: x_dtype must be MOE_BF16 (the rows it reads)");
+    if (dims->H % 128 != 0)
+        return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_fused_quant: H=%d must be a multiple of 128", dims->H);
+    const char *why = fused_quant_unsupported(dims->N, dims->T, dims->E, dims->R);
+    if (why[0] != '\0')
+        return set_error(MOE_ERR_UNSUPPORTED, "moe_dispatch_fused_quant: %s; use the separate calls", why);
+    // an empty batch touches no workspace (its size is 0 there): NULL is fine
+    if (!expert_counts || !expert_offsets || !rank_counts || !rank_offsets || !send_counts || !status ||
+        (!workspace && v.NT > 0))
+        return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_fused_quant: a required pointer is NULL");
+    if (v.NT > 0 && (!logits || !x || !topk_idx || !topk_w || !pos || !packed_q || !packed_scales || !packed_src))
+        return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_fused_quant: a required pointer is NULL");
+    if ((x && !aligned(x, 16)) || (packed_q && !aligned(packed_q, 16)) || (workspace && !aligned(workspace, 16)))
+        return set_error(MOE_ERR_INVALID_ARG,
+                         "moe_dispatch_fused_quant: x, packed_q and workspace must be 16-byte aligned");
+    const void *ptrs4[] = {logits, bias, topk_idx, topk_w, expert_counts, expert_offsets, rank_counts,
+                           rank_offsets, send_counts, pos, status, packed_scales, packed_src};
+    for (const void *p : ptrs4)
+        if (p && !aligned(p, 4))
+            return set_error(MOE_ERR_INVALID_ARG, "moe_dispatch_fused_quant: pointers must be 4-byte aligned");
+    return cuda_result(launch_dispatch_fused_quant(logits, bias, score_fn, renormalize ? 1 : 0, x, dims->N, dims->T,
+                                                   dims->E, dims->R, dims->H, v.cap, topk_idx, topk_w,
+                                                   expert_counts, expert_offsets, rank_counts, rank_offsets,
+                                                   send_counts, pos, status, packed_q, packed_scales, packed_src,
+                                                   workspace, (cudaStream_t)stream),
+                       "moe_dispatch_fused_quant");
+}
+
 int moe_dispatch_fused_static(const MoeDims *dims, const float *logits, const float *bias, int score_fn,
                               int renormalize, const void *x, const float *x_scales, int32_t *topk_idx,
                               float *topk_w, int32_t *expert_counts, int32_t *expert_offsets,

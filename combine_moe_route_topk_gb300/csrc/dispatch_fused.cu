@@ -391,6 +391,63 @@ const char *two_kernel_unsupported(int N, int T, int E, int R) {
 
 }  // namespace
 
+// Kernel 1 of the two-kernel form; fills *D with what the pack kernel needs
+// to derive the rows.
+static cudaError_t launch_route_hist(const float *logits, const float *bias, int score_fn, int renormalize, int N, int T,
+                              int E, int R, int64_t cap, int32_t *topk_idx, float *topk_w, int32_t *expert_counts,
+                              int32_t *expert_offsets, int32_t *rank_counts, int32_t *rank_offsets,
+                              int32_t *send_counts, int32_t *pos, int32_t *status, void *workspace,
+                              cudaStream_t stream, PackDerive *D) {
+    FusedParams P;
+    P.logits = logits;
+    P.bias = bias;
+    P.score_fn = score_fn;
+    P.renormalize = renormalize;
+    P.N = N;
+    P.T = T;
+    P.E = E;
+    P.R = R;
+    P.cap = (int)cap;
+    P.geo = fused_geom(N, T);
+    P.topk_idx = topk_idx;
+    P.topk_w = topk_w;
+    P.expert_counts = expert_counts;
+    P.expert_offsets = expert_offsets;
+    P.rank_counts = rank_counts;
+    P.rank_offsets = rank_offsets;
+    P.send_counts = send_counts;
+    P.pos = pos;
+    P.status = status;
+    P.ws = reinterpret_cast<unsigned char *>(workspace);
+    const int need = (E + 31) / 32;
+    // the same experts per lane as the route kernel, so that the softmax
+    // denominator is summed in the same order and the weights agree bit for bit
+    cudaError_t e;
+    if (need <= 1) e = launch_route_hist_j<1>(P, stream);
+    else if (need <= 2) e = launch_route_hist_j<2>(P, stream);
+    else if (need <= 4) e = launch_route_hist_j<4>(P, stream);
+    else if (need <= 8) e = launch_route_hist_j<8>(P, stream);
+    else if (need <= 12) e = launch_route_hist_j<12>(P, stream);
+    else e = launch_route_hist_j<16>(P, stream);
+    if (e != cudaSuccess) return e;
+    const WsLayout wl = ws_layout(N, T, E);
+    D->topk_idx = topk_idx;
+    D->expert_offsets = expert_offsets;
+    D->chunk_prefix = reinterpret_cast<const uint16_t *>(P.ws + wl.cpre);
+    D->block_hist = P.ws + wl.hist;
+    D->block_send = reinterpret_cast<const uint16_t *>(P.ws + wl.sd);
+    D->send_counts = send_counts;
+    D->N = N;
+    D->T = T;
+    D->ranks_per_block = P.geo.rpb;
+    D->blocks_per_rank = P.geo.cps;
+    D->L = E / N;
+    D->Ep = pad16(E);
+    D->cap = (int)cap;
+    D->route_blocks = P.geo.B;
+    return cudaSuccess;
+}
+
 int64_t fused_workspace_bytes(int N, int T, int E) {
     if ((int64_t)N * T == 0 || two_kernel_unsupported(N, T, E, 1)[0] != '\0') return 0;
     return ws_layout(N, T, E).bytes;
@@ -427,55 +484,37 @@ cudaError_t launch_dispatch_fused(const float *logits, const float *bias, int sc
         if (e != cudaErrorNotSupported) return e;
         if (two_kernel_unsupported(N, T, E, R)[0] != '\0') return cudaErrorNotSupported;
     }
-    FusedParams P;
-    P.logits = logits;
-    P.bias = bias;
-    P.score_fn = score_fn;
-    P.renormalize = renormalize;
-    P.N = N;
-    P.T = T;
-    P.E = E;
-    P.R = R;
-    P.cap = (int)cap;
-    P.geo = fused_geom(N, T);
-    P.topk_idx = topk_idx;
-    P.topk_w = topk_w;
-    P.expert_counts = expert_counts;
-    P.expert_offsets = expert_offsets;
-    P.rank_counts = rank_counts;
-    P.rank_offsets = rank_offsets;
-    P.send_counts = send_counts;
-    P.pos = pos;
-    P.status = status;
-    P.ws = reinterpret_cast<unsigned char *>(workspace);
-    const int need = (E + 31) / 32;
-    // the same experts per lane as the route kernel, so that the softmax
-    // denominator is summed in the same order and the weights agree bit for bit
-    cudaError_t e;
-    if (need <= 1) e = launch_route_hist_j<1>(P, stream);
-    else if (need <= 2) e = launch_route_hist_j<2>(P, stream);
-    else if (need <= 4) e = launch_route_hist_j<4>(P, stream);
-    else if (need <= 8) e = launch_route_hist_j<8>(P, stream);
-    else if (need <= 12) e = launch_route_hist_j<12>(P, stream);
-    else e = launch_route_hist_j<16>(P, stream);
-    if (e != cudaSuccess) return e;
     PackDerive D;
-    D.topk_idx = topk_idx;
-    D.expert_offsets = expert_offsets;
-    D.chunk_prefix = reinterpret_cast<const uint16_t *>(P.ws + ws_layout(N, T, E).cpre);
-    D.block_hist = P.ws + ws_layout(N, T, E).hist;
-    D.block_send = reinterpret_cast<const uint16_t *>(P.ws + ws_layout(N, T, E).sd);
-    D.send_counts = send_counts;
-    D.N = N;
-    D.T = T;
-    D.ranks_per_block = P.geo.rpb;
-    D.blocks_per_rank = P.geo.cps;
-    D.L = E / N;
-    D.Ep = pad16(E);
-    D.cap = (int)cap;
-    D.route_blocks = P.geo.B;
+    cudaError_t e = launch_route_hist(logits, bias, score_fn, renormalize, N, T, E, R, cap, topk_idx, topk_w,
+                                      expert_counts, expert_offsets, rank_counts, rank_offsets, send_counts, pos,
+                                      status, workspace, stream, &D);
+    if (e != cudaSuccess) return e;
     return launch_dispatch_pack_derive(x, x_scales, pos, (int64_t)N * T, R, row_bytes, spr, (int64_t)N * cap, D,
                                        packed_x, packed_scales, packed_src, stream);
+}
+
+const char *fused_quant_unsupported(int N, int T, int E, int R) {
+    if ((int64_t)N * T == 0) return "";
+    return two_kernel_unsupported(N, T, E, R);
+}
+
+cudaError_t launch_dispatch_fused_quant(const float *logits, const float *bias, int score_fn, int renormalize,
+                                        const void *x, int N, int T, int E, int R, int H, int64_t cap,
+                                        int32_t *topk_idx, float *topk_w, int32_t *expert_counts,
+                                        int32_t *expert_offsets, int32_t *rank_counts, int32_t *rank_offsets,
+                                        int32_t *send_counts, int32_t *pos, int32_t *status, void *packed_q,
+                                        float *packed_scales, int32_t *packed_src, void *workspace,
+                                        cudaStream_t stream) {
+    if ((int64_t)N * T == 0)
+        return launch_dispatch_count(topk_idx, N, T, E, R, cap, expert_counts, expert_offsets, rank_counts,
+                                     rank_offsets, send_counts, pos, status, stream);
+    PackDerive D;
+    cudaError_t e = launch_route_hist(logits, bias, score_fn, renormalize, N, T, E, R, cap, topk_idx, topk_w,
+                                      expert_counts, expert_offsets, rank_counts, rank_offsets, send_counts, pos,
+                                      status, workspace, stream, &D);
+    if (e != cudaSuccess) return e;
+    return launch_dispatch_pack_quant_derive(x, pos, (int64_t)N * T, R, H, (int64_t)N * cap, D, packed_q,
+                                             packed_scales, packed_src, stream);
 }
 
 }  // namespace moe

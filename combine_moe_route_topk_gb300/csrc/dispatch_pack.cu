@@ -29,6 +29,7 @@
 // The decode-fused dispatch launches the same kernel in a second form that
 // computes each pair's row itself from the per-block ranks and prefixes of
 // the fused route kernel (PackDerive) and writes it to pos.
+#include "fused_rows.cuh"
 #include "mem_ops.cuh"
 #include "moe_internal.cuh"
 #include "pdl.cuh"
@@ -121,15 +122,7 @@ dispatch_pack_derive_kernel(const uint4 *__restrict__ x, const float *__restrict
     prefetch_rows_l2(x, (int64_t)nvec * 16, pf_rows, pf_blocks);  // before the wait: hints only
     grid_dependency_wait();  // ranks and prefixes come from the fused route kernel
     grid_launch_dependents();
-    if (D.blocks_per_rank > 0 && (int)blockIdx.x < D.N) {
-        // row s of send_counts: the counts of the blocks of source rank s
-        const int s = (int)blockIdx.x, cps = D.blocks_per_rank;
-        for (int d = tid; d < D.N; d += nthr) {
-            int c = 0;
-            for (int k = 0; k < cps; ++k) c += __ldg(D.block_send + (int64_t)(s * cps + k) * D.N + d);
-            D.send_counts[(int64_t)s * D.N + d] = c;
-        }
-    }
+    fused_send_counts(D);
     const uint64_t stream_out = l2_policy_evict_first();
     for (int64_t g0 = (int64_t)blockIdx.x * kTok; g0 < NT; g0 += (int64_t)gridDim.x * kTok) {
         for (int i = tid; i < kTok * R; i += nthr) {
@@ -137,22 +130,7 @@ dispatch_pack_derive_kernel(const uint4 *__restrict__ x, const float *__restrict
             const int64_t g = g0 + u;
             int p = -1;
             if (g < NT) {
-                // row = d*cap + (start of expert e within rank d) + pairs of e in
-                // earlier chunks and earlier blocks of this chunk + rank among
-                // this block's pairs of e
-                const int e = __ldg(D.topk_idx + g * R + k);
-                const int r = pos[g * R + k];
-                const int gi = (int)g;
-                const int b = D.ranks_per_block > 0 ? gi / (D.ranks_per_block * D.T)
-                                                    : (gi / D.T) * D.blocks_per_rank + (gi % D.T) / 32;
-                const int d = e / D.L;
-                const int c0 = b & ~7;  // first block of b's chunk of 8
-                int local = __ldg(D.expert_offsets + e) - __ldg(D.expert_offsets + d * D.L) +
-                            (int)__ldg(D.chunk_prefix + (int64_t)(b >> 3) * D.Ep + e) + r;
-#pragma unroll
-                for (int j = 0; j < 7; ++j)
-                    if (c0 + j < b) local += __ldg(D.block_hist + (int64_t)(c0 + j) * D.Ep + e);
-                p = local < D.cap ? d * D.cap + local : -1;
+                p = fused_row(D, g, __ldg(D.topk_idx + g * R + k), pos[g * R + k]);
                 pos[g * R + k] = p;
                 if (p >= 0 && (int64_t)p < rows_total) packed_src[p] = (int32_t)(g * R + k);
                 else p = -1;

@@ -66,6 +66,10 @@ cudaError_t launch_dispatch_pack_derive(const void *x, const float *x_scales, in
                                         int R, int64_t row_bytes, int scales_per_row, int64_t rows_total,
                                         const PackDerive &D, void *packed_x, float *packed_scales,
                                         int32_t *packed_src, cudaStream_t stream);
+// The fp8-quantising pack in the same deriving form (bf16 rows in).
+cudaError_t launch_dispatch_pack_quant_derive(const void *x, int32_t *pos, int64_t NT, int R, int H,
+                                              int64_t rows_total, const PackDerive &D, void *packed_q,
+                                              float *packed_scales, int32_t *packed_src, cudaStream_t stream);
 // Rows of x the pack prefetches into L2 (at most half the L2; 0 for rows
 // wider than one bulk prefetch).
 int64_t pack_prefetch_rows(int64_t NT, int64_t row_bytes);
@@ -93,6 +97,17 @@ cudaError_t launch_dispatch_fused(const float *logits, const float *bias, int sc
                                   int32_t *rank_counts, int32_t *rank_offsets, int32_t *send_counts,
                                   int32_t *pos, int32_t *status, void *packed_x, float *packed_scales,
                                   int32_t *packed_src, void *workspace, cudaStream_t stream);
+
+// Decode-fused route + count + fp8-quantising pack (bf16 rows in; always the
+// two-kernel form).  "" when the batch is within its limits.
+const char *fused_quant_unsupported(int N, int T, int E, int R);
+cudaError_t launch_dispatch_fused_quant(const float *logits, const float *bias, int score_fn, int renormalize,
+                                        const void *x, int N, int T, int E, int R, int H, int64_t cap,
+                                        int32_t *topk_idx, float *topk_w, int32_t *expert_counts,
+                                        int32_t *expert_offsets, int32_t *rank_counts, int32_t *rank_offsets,
+                                        int32_t *send_counts, int32_t *pos, int32_t *status, void *packed_q,
+                                        float *packed_scales, int32_t *packed_src, void *workspace,
+                                        cudaStream_t stream);
 
 // Small decode batches: route + count + pack in one thread-block cluster.
 bool dispatch_small_eligible(int64_t NT, int E, int R, int64_t row_bytes);

@@ -261,3 +261,18 @@ def test_fused_workspace_fits_the_static_scratch_and_is_zero_outside_the_fused_s
     # no fused form with a workspace takes these: more than 4096 tokens, E > 512
     assert moe.buffer_sizes(moe.make_dims(4, 4096, 128, 8, 64))["fused_workspace_bytes"] == 0
     assert moe.buffer_sizes(moe.make_dims(4, 64, 1024, 8, 64))["fused_workspace_bytes"] == 0
+
+
+@pytest.mark.parametrize("kw,code,msg", [
+    (dict(N=4, T=64, E=64, R=8, H=128, x_dtype=moe.MOE_F32), moe.MOE_ERR_INVALID_ARG, "MOE_BF16"),
+    (dict(N=4, T=64, E=64, R=8, H=136), moe.MOE_ERR_INVALID_ARG, "multiple of 128"),
+    (dict(N=4, T=4096, E=64, R=8, H=128), moe.MOE_ERR_UNSUPPORTED, "4096"),
+    (dict(N=4, T=64, E=1024, R=8, H=128), moe.MOE_ERR_UNSUPPORTED, "E > 512")])
+def test_fused_quant_dispatch_rejects_bad_rows_and_non_decode_batches(lib, kw, code, msg):
+    P = ctypes.c_void_p
+    ok = P(0x10000)
+    d = moe.make_dims(**kw)
+    # logits, bias, score_fn, renormalize, x, then topk_idx .. packed_src
+    # (12 pointers), the workspace and the stream
+    assert lib.moe_dispatch_fused_quant(ctypes.byref(d), ok, None, 0, 0, ok, *([ok] * 12), ok, None) == code
+    assert msg in lib.moe_last_error().decode()

@@ -25,7 +25,10 @@ def _built():
     _build.build()
 
 
-def _run(w, inp, special=None):
+def _run(w, inp, special=None, fused=False):
+    """fused: moe_dispatch_fused_quant (route, count and the quantising pack
+    in one call) in place of the three calls; its routing, counts and rows are
+    checked against the oracle as well."""
     dims = moe.dims_of(w)
     dev = torch.device("cuda", torch.cuda.current_device())
     b = moe.Buffers(dims, device=dev)
@@ -35,13 +38,20 @@ def _run(w, inp, special=None):
     q = moe.buffer_sizes(moe.fp8_dims(dims))
     packed_q = torch.empty(q["packed_x_bytes"], dtype=torch.uint8, device=dev)
     packed_scales = torch.empty(q["packed_scales_bytes"] // 4, dtype=torch.float32, device=dev)
-    moe.route_topk(dims, logits, bias, w.score_fn, w.renormalize, b.topk_idx, b.topk_w)
-    moe.dispatch_count(dims, b.topk_idx, b.expert_counts, b.expert_offsets, b.rank_counts,
-                       b.rank_offsets, b.send_counts, b.pos, b.status)
     pq2 = packed_q.view(-1, w.H)
     ps2 = packed_scales.view(-1, w.H // 128)
     fill_sentinels(pq2, ps2, b.packed_src)
-    moe.dispatch_pack_quant(dims, x, b.pos, packed_q, packed_scales, b.packed_src)
+    if fused:
+        ws = torch.zeros(b.sizes["fused_workspace_bytes"], dtype=torch.uint8, device=dev)
+        moe.dispatch_fused_quant(dims, logits, bias, w.score_fn, w.renormalize, x, b.topk_idx,
+                                 b.topk_w, b.expert_counts, b.expert_offsets, b.rank_counts,
+                                 b.rank_offsets, b.send_counts, b.pos, b.status, packed_q,
+                                 packed_scales, b.packed_src, ws)
+    else:
+        moe.route_topk(dims, logits, bias, w.score_fn, w.renormalize, b.topk_idx, b.topk_w)
+        moe.dispatch_count(dims, b.topk_idx, b.expert_counts, b.expert_offsets, b.rank_counts,
+                           b.rank_offsets, b.send_counts, b.pos, b.status)
+        moe.dispatch_pack_quant(dims, x, b.pos, packed_q, packed_scales, b.packed_src)
     assert moe.read_status(b.status) == moe.MOE_OK
     cap = b.sizes["cap_rows"]
     rank_counts = b.rank_counts.cpu().numpy()
@@ -55,6 +65,10 @@ def _run(w, inp, special=None):
                              w.R, w.score_fn, w.renormalize)
     cnt, st = oracle.count(w.N, w.T, w.E, cap, idx)
     assert st == oracle.OK
+    if fused:
+        np.testing.assert_array_equal(b.topk_idx.cpu().numpy(), idx)
+        for k in ("expert_counts", "expert_offsets", "rank_counts", "rank_offsets", "send_counts", "pos"):
+            np.testing.assert_array_equal(getattr(b, k).cpu().numpy(), cnt[k], err_msg=k)
     codes, scales = oracle.quantize_rows(inp.x)
     oq, osc, osrc = oracle.pack(codes, scales, cnt["pos"], cnt["rank_offsets"], cap)
     crow = compact_of_region(rows, cap, cnt["rank_offsets"])
@@ -99,3 +113,35 @@ def test_quant_pack_zero_blocks_tiny_values_and_signed_zeros():
     x[:, 386] = 50.0
     inp.x = x.to(torch.bfloat16)
     _run(w, inp)
+
+
+# the decode-fused form (moe_dispatch_fused_quant): the same checks plus its
+# routing and counts against the oracle
+@pytest.mark.parametrize("name", ["dsv3_decode", "kimi_k2_decode"])
+def test_fused_quant_full_size(name):
+    w = W.WORKLOADS[name]
+    _run(w, W.make_inputs(w), fused=True)
+
+
+@pytest.mark.parametrize("N,T,E,R,H", [(3, 77, 24, 3, 128), (4, 50, 32, 5, 384),
+                                       (2, 300, 16, 2, 1152), (2, 24, 8, 3, 36864),
+                                       (124, 33, 496, 8, 128)])
+def test_fused_quant_ragged(N, T, E, R, H):
+    w = W.Workload("fq", N=N, T=T, E=E, R=R, H=H, score_fn=W.SIGMOID, bias="normal",
+                   renormalize=True, seed=N + T)
+    _run(w, W.make_inputs(w), fused=True)
+
+
+def test_fused_quant_rejects_other_rows_and_non_decode_batches():
+    w = W.Workload("fqx", N=2, T=64, E=8, R=2, H=256, x_dtype=W.F32, seed=1)
+    dims = moe.dims_of(w)
+    b = moe.Buffers(dims)
+    inp = W.make_inputs(w, device="cuda")
+    q = moe.buffer_sizes(moe.fp8_dims(dims))
+    pq = torch.empty(q["packed_x_bytes"], dtype=torch.uint8, device="cuda")
+    ps = torch.empty(q["packed_scales_bytes"] // 4, dtype=torch.float32, device="cuda")
+    ws = torch.zeros(max(16, b.sizes["fused_workspace_bytes"]), dtype=torch.uint8, device="cuda")
+    with pytest.raises((moe.MoeError, ValueError)):  # f32 rows: the binding or the library refuses
+        moe.dispatch_fused_quant(dims, inp.logits, None, w.score_fn, False, inp.x, b.topk_idx, b.topk_w,
+                                 b.expert_counts, b.expert_offsets, b.rank_counts, b.rank_offsets,
+                                 b.send_counts, b.pos, b.status, pq, ps, b.packed_src, ws)
