@@ -3,7 +3,8 @@ bar of its own tests:
 
 * decode-fused dispatch (both the single-cluster and the two-kernel form)
   against the three separate calls, byte for byte;
-* the quantising pack against the oracle (codes and scales bit-exact);
+* the quantising pack against the oracle (codes and scales bit-exact), also
+  through the decode-fused fp8 dispatch (routing and counts too);
 * the expert-parallel local path of a rank and the send-side partials
   against the oracle;
 * the bias-for-selection-only router against the oracle (near-tie rule).
@@ -128,6 +129,34 @@ def _quant_shapes(n, seed=37):
 @pytest.mark.parametrize("w", _quant_shapes(S.count(10), S.seed(37)), ids=lambda w: w.name)
 def test_random_quant_pack(w):
     run_quant(w, W.make_inputs(w))
+
+
+def _fused_quant_shapes(n, seed=39):
+    """Decode batches for moe_dispatch_fused_quant: up to 4096 tokens, E up to
+    512, any T and R, bf16 rows of 128-element blocks."""
+    rng = random.Random(seed)
+    out = []
+    for i in range(n):
+        N = rng.choice([1, 2, 4, 8, 16, 32, 64])
+        E = N * rng.choice([1, 2, 3, 5, 8])
+        while E > 512:
+            E //= 2
+        E = max(N, E // N * N)
+        R = rng.randint(1, min(E, 32))
+        T = rng.randint(1, max(1, min(256, 4096 // N)))
+        out.append(W.Workload(f"fquant{i}", N=N, T=T, E=E, R=R, H=128 * rng.randint(1, 8),
+                              score_fn=rng.choice([W.SOFTMAX, W.SIGMOID]),
+                              renormalize=rng.random() < 0.5, bias=rng.choice(["none", "normal"]),
+                              seed=3500 + i))
+    return out
+
+
+@pytest.mark.parametrize("w", _fused_quant_shapes(S.count(10), S.seed(39)), ids=lambda w: w.name)
+def test_random_fused_quant(w):
+    # routing, counts, positions, codes, scales and rows against the oracle
+    # (the default reading of the bias: selection on exact f32 keys, so the
+    # indices are compared bit for bit)
+    run_quant(w, W.make_inputs(w), fused=True)
 
 
 def _rank_shapes(n, seed=41):
