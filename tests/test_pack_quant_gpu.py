@@ -145,3 +145,52 @@ def test_fused_quant_rejects_other_rows_and_non_decode_batches():
         moe.dispatch_fused_quant(dims, inp.logits, None, w.score_fn, False, inp.x, b.topk_idx, b.topk_w,
                                  b.expert_counts, b.expert_offsets, b.rank_counts, b.rank_offsets,
                                  b.send_counts, b.pos, b.status, pq, ps, b.packed_src, ws)
+
+
+def _quant_dispatch(w, inp, fused):
+    """Every output of the fp8 dispatch, as the three calls or as one."""
+    dims = moe.dims_of(w)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    b = moe.Buffers(dims, device=dev)
+    q = moe.buffer_sizes(moe.fp8_dims(dims))
+    pq = torch.zeros(q["packed_x_bytes"], dtype=torch.uint8, device=dev)
+    ps = torch.zeros(q["packed_scales_bytes"] // 4, dtype=torch.float32, device=dev)
+    for t in (b.topk_idx, b.topk_w, b.expert_counts, b.expert_offsets, b.rank_counts, b.rank_offsets,
+              b.send_counts, b.pos, b.status, b.packed_src):
+        t.view(torch.uint8).zero_()
+    logits, x = inp.logits.to(dev), inp.x.to(dev)
+    bias = None if inp.bias is None else inp.bias.to(dev)
+    if fused:
+        ws = torch.zeros(b.sizes["fused_workspace_bytes"], dtype=torch.uint8, device=dev)
+        moe.dispatch_fused_quant(dims, logits, bias, w.score_fn, w.renormalize, x, b.topk_idx, b.topk_w,
+                                 b.expert_counts, b.expert_offsets, b.rank_counts, b.rank_offsets,
+                                 b.send_counts, b.pos, b.status, pq, ps, b.packed_src, ws)
+    else:
+        moe.route_topk(dims, logits, bias, w.score_fn, w.renormalize, b.topk_idx, b.topk_w)
+        moe.dispatch_count(dims, b.topk_idx, b.expert_counts, b.expert_offsets, b.rank_counts,
+                           b.rank_offsets, b.send_counts, b.pos, b.status)
+        moe.dispatch_pack_quant(dims, x, b.pos, pq, ps, b.packed_src)
+    torch.cuda.synchronize()
+    out = {k: getattr(b, k).cpu().numpy() for k in ("topk_idx", "topk_w", "expert_counts", "expert_offsets",
+                                                     "rank_counts", "rank_offsets", "send_counts", "pos",
+                                                     "status", "packed_src")}
+    out["packed_q"] = pq.cpu().numpy()
+    out["packed_scales"] = ps.cpu().numpy().view(np.uint32)
+    return out
+
+
+@pytest.mark.parametrize("w", [
+    # capacity overflow: rows past a rank's 300 are dropped (pos = -1)
+    W.Workload("fq_cap", N=8, T=96, E=32, R=4, H=256, cap_rows=300, seed=201),
+    # the DeepSeek-V3 convention of the bias (selection only)
+    W.Workload("fq_bsel", N=16, T=64, E=256, R=8, H=384, score_fn=W.SIGMOID | moe.MOE_BIAS_SELECT_ONLY,
+               bias="normal", renormalize=True, seed=202),
+], ids=lambda w: w.name)
+def test_fused_quant_equals_the_three_calls_bytewise(w):
+    inp = W.make_inputs(w)
+    a = _quant_dispatch(w, inp, fused=True)
+    b = _quant_dispatch(w, inp, fused=False)
+    for k in a:
+        np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+    if w.name == "fq_cap":
+        assert int(a["status"][0]) == moe.MOE_ERR_CAPACITY
